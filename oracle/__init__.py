@@ -1,0 +1,12 @@
+"""CPU oracle for the MoE layer forward (test infrastructure only).
+
+Importable by ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline / reference arm; never by the product path.
+"""
+from .moe_oracle import (DEFAULT, RENORMALIZE, DEEPSEEKV3, RENORMALIZE_NAIVE, SIGMOID_RENORM,
+                         METHODS, topk_desc, softmax64, sigmoid64, deepseek_keys, group_select,
+                         route, permute, swiglu, expert_ffn, forward, forward_permuted)
+
+__all__ = ["DEFAULT", "RENORMALIZE", "DEEPSEEKV3", "RENORMALIZE_NAIVE", "SIGMOID_RENORM",
+           "METHODS", "topk_desc", "softmax64", "sigmoid64", "deepseek_keys", "group_select",
+           "route", "permute", "swiglu", "expert_ffn", "forward", "forward_permuted"]

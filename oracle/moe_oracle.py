@@ -1,0 +1,247 @@
+"""CPU oracle for the MoE layer forward -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its CPU-baseline
+leg and its ``--impl reference`` arm) may import this module. The product path
+(the C-ABI library and its Python binding) never calls it, and it shares no
+code, table or helper with that path.
+
+Plain, slow, obviously correct: numpy in float64, one step per definition,
+no blocking or fusion. Sources (titles of the pages that define the method):
+
+* [TRT] "TensorRT-LLM 源码完全拆解(十三): MoE 层前向执行——路由、Fused Kernel 与专家并行的三段拼装"
+* [VLLM] "vLLM 源码完全拆解(八): MoE 层的前向执行"
+* [GG] "从 Dense GEMM 到 TP MoE 的演进逻辑" (gsyq.cn news 428989), a GroupedGEMM / TP-MoE article
+
+The layer computes (TRT, section "MoE 在推理侧到底特殊在哪里", the MoE formula)
+
+    y = sum_{i in TopK(x)} g_i(x) * E_i(x)  (+ shared expert, TRT layer-structure figure)
+
+with E_i a SwiGLU FFN. Readings taken where the pages are silent:
+
+* Selection for the softmax/sigmoid methods is top-k of the raw fp32 logit
+  (softmax and sigmoid are strictly increasing, so the chosen set and its order
+  are those of the scores); ties go to the lowest expert index.
+* DeepSeek-V3 selection key: kappa_e = fl32(fl32(sigmoid64(l_e)) + b_e), i.e.
+  the sigmoid in float64 rounded once to fp32, then an IEEE fp32 add of the
+  bias. Group score = fl32(top1 + top2 of kappa within the group). Ties: lowest
+  group index, then lowest expert index.
+* Output slots are listed by descending selection key.
+* SwiGLU: the first I rows of w13[e] are the gate projection (w1), the next I
+  rows the up projection (w3): h = silu(gate) * up, silu(z) = z / (1 + e^-z).
+* The shared expert enters with weight 1 (the routed scaling factor is already
+  inside the routed scales).
+* Non-finite logits count as -inf for selection and for the normalisers.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+DEFAULT = 0
+RENORMALIZE = 1
+DEEPSEEKV3 = 2
+RENORMALIZE_NAIVE = 4
+SIGMOID_RENORM = 6
+
+METHODS = (DEFAULT, RENORMALIZE, DEEPSEEKV3, RENORMALIZE_NAIVE, SIGMOID_RENORM)
+
+
+# --------------------------------------------------------------------------- routing
+
+def topk_desc(keys: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest keys per row, largest first, ties -> lowest index.
+
+    A stable sort of the negated keys keeps equal keys in ascending index order.
+    """
+    return np.argsort(-keys, axis=-1, kind="stable")[..., :k]
+
+
+def _selection_logits(logits32: np.ndarray) -> np.ndarray:
+    return np.where(np.isfinite(logits32), logits32, np.float32(-np.inf)).astype(np.float32)
+
+
+def softmax64(l: np.ndarray) -> np.ndarray:
+    """Row softmax in float64; -inf entries get probability 0."""
+    m = np.max(l, axis=-1, keepdims=True)
+    z = np.exp(l - m)
+    return z / np.sum(z, axis=-1, keepdims=True)
+
+
+def sigmoid64(l: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-l))
+
+
+def deepseek_keys(logits32: np.ndarray, bias32: np.ndarray):
+    """(unbiased sigmoid scores in float64, fp32 selection keys kappa).
+
+    TRT, section "DeepSeek-V3 的 noaux_tc:分组路由的算术": scores = sigmoid(logits),
+    scores_with_bias = scores + e_score_correction_bias; the bias only decides who is
+    chosen, the weights use the unbiased scores.
+    """
+    l = _selection_logits(logits32)
+    s64 = sigmoid64(l.astype(np.float64))
+    kappa = (s64.astype(np.float32) + bias32.astype(np.float32)).astype(np.float32)
+    return s64, kappa
+
+
+def group_select(kappa: np.ndarray, n_group: int, topk_group: int):
+    """Chosen groups per token (group-score descending) and the group scores.
+
+    TRT noaux_tc section: group score = sum of the top-2 biased scores inside the
+    group; keep the topk_group best groups.
+    """
+    T, E = kappa.shape
+    epg = E // n_group
+    g = kappa.reshape(T, n_group, epg)
+    top2 = -np.sort(-g, axis=-1)[..., :2]
+    gscore = (top2[..., 0] + top2[..., 1]).astype(np.float32)
+    groups = topk_desc(gscore, topk_group)
+    return groups, gscore
+
+
+def route(logits, method: int, top_k: int, bias=None, n_group: int = 1, topk_group: int = 1,
+          routed_scaling_factor: float = 1.0):
+    """Routing: logits [T, E] fp32 -> (ids int32 [T, k], scales float64 [T, k]).
+
+    TRT, section "路由方法枚举" (RoutingMethodType):
+      Default (0)           softmax -> top-k, weights = selected softmax probabilities
+      Renormalize (1)       top-k -> softmax over the selected logits
+      DeepSeekV3 (2)        sigmoid -> bias add -> top-2 per group -> top groups -> top-k
+      RenormalizeNaive (4)  softmax -> top-k -> divide by the selected sum
+      SigmoidRenorm (6)     sigmoid -> top-k -> divide by the selected sum
+    VLLM, section "FusedTopKRouter": the same softmax/sigmoid -> top-k -> renormalize.
+    """
+    l32 = np.asarray(logits, dtype=np.float32)
+    T, E = l32.shape
+    sel = _selection_logits(l32)
+    l64 = sel.astype(np.float64)
+    if method in (DEFAULT, RENORMALIZE, RENORMALIZE_NAIVE, SIGMOID_RENORM):
+        ids = topk_desc(sel, top_k)
+        lsel = np.take_along_axis(l64, ids, axis=1)
+        if method == DEFAULT:
+            # The normaliser covers all E experts (TRT: Default vs Renormalize differ only
+            # in which experts the denominator includes).
+            w = np.take_along_axis(softmax64(l64), ids, axis=1)
+        elif method == RENORMALIZE:
+            w = softmax64(lsel)
+        elif method == RENORMALIZE_NAIVE:
+            p = np.take_along_axis(softmax64(l64), ids, axis=1)
+            w = p / np.sum(p, axis=1, keepdims=True)
+        else:
+            s = sigmoid64(lsel)
+            w = s / np.sum(s, axis=1, keepdims=True)
+        return ids.astype(np.int32), w
+    if method == DEEPSEEKV3:
+        b = np.zeros(E, np.float32) if bias is None else np.asarray(bias, np.float32)
+        s64, kappa = deepseek_keys(l32, b)
+        groups, _ = group_select(kappa, n_group, topk_group)
+        epg = E // n_group
+        in_group = np.zeros((T, n_group), dtype=bool)
+        np.put_along_axis(in_group, groups, True, axis=1)
+        mask = np.repeat(in_group, epg, axis=1)
+        masked = np.where(mask, kappa, np.float32(-np.inf))
+        ids = topk_desc(masked, top_k)
+        ssel = np.take_along_axis(s64, ids, axis=1)
+        w = ssel / (np.sum(ssel, axis=1, keepdims=True) + 1e-20) * routed_scaling_factor
+        return ids.astype(np.int32), w
+    raise ValueError(f"unsupported routing method {method}")
+
+
+# --------------------------------------------------------------------------- permute
+
+def permute(ids: np.ndarray, E: int):
+    """Group the T*k (token, slot) pairs into contiguous per-expert blocks.
+
+    GG section 2.1/2.2: all experts' rows are concatenated with an offset array;
+    tokens are permuted so each expert's rows are contiguous. Within an expert the
+    rows keep ascending flat index f = t*k + j (stable).
+    Returns counts [E], offsets [E+1], perm_src [P] (position -> f), perm_inv [P].
+    """
+    flat = np.asarray(ids, dtype=np.int64).reshape(-1)
+    counts = np.bincount(flat, minlength=E)[:E]
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    perm_src = np.argsort(flat, kind="stable")
+    perm_inv = np.empty_like(perm_src)
+    perm_inv[perm_src] = np.arange(flat.size)
+    return (counts.astype(np.int32), offsets.astype(np.int32), perm_src.astype(np.int32),
+            perm_inv.astype(np.int32))
+
+
+# --------------------------------------------------------------------------- experts
+
+def swiglu(a: np.ndarray, I: int) -> np.ndarray:
+    """h = silu(gate) * up with gate = a[:, :I], up = a[:, I:2I]."""
+    g, u = a[:, :I], a[:, I:2 * I]
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g)) * u
+
+
+def expert_ffn(X: np.ndarray, w13e, w2e) -> np.ndarray:
+    """One SwiGLU expert on rows X [m, H]: w2e [H, I] . swiglu(w13e [2I, H] . x).
+
+    VLLM, section "专家权重如何存储": w13 = gate and up merged, [2I, H]; w2 = down, [H, I].
+    """
+    w13e = np.asarray(w13e, dtype=np.float64)
+    w2e = np.asarray(w2e, dtype=np.float64)
+    I = w2e.shape[1]
+    a = X @ w13e.T
+    h = swiglu(a, I)
+    return h @ w2e.T
+
+
+def forward(x, ids, scales, w13, w2, w13_s=None, w2_s=None) -> np.ndarray:
+    """y [T, H] float64 = sum_j scales[t, j] * E_{ids[t, j]}(x[t]) (+ shared(x[t])).
+
+    ``w13``/``w2`` are indexable per expert (``w13[e]`` -> [2I, H]), so callers can
+    hand over one expert at a time. Tokens are independent: passing a subset of
+    rows of x/ids/scales gives the matching rows of y.
+    """
+    X = np.asarray(x, dtype=np.float64)
+    ids = np.asarray(ids)
+    scales = np.asarray(scales, dtype=np.float64)
+    T, H = X.shape
+    y = np.zeros((T, H), dtype=np.float64)
+    for e in np.unique(ids):
+        rows, slots = np.nonzero(ids == e)
+        o = expert_ffn(X[rows], w13[int(e)], w2[int(e)])
+        np.add.at(y, rows, scales[rows, slots][:, None] * o)
+    if w13_s is not None:
+        y += expert_ffn(X, w13_s, w2_s)
+    return y
+
+
+def forward_permuted(x, ids, scales, w13, w2, w13_s=None, w2_s=None):
+    """The same result computed in the five-step order of the pages.
+
+    route (given) -> permute -> per-expert FC1 + SwiGLU -> FC2 -> finalize (unpermute and
+    apply the routing weights after FC2, TRT section on finalize before/after combine).
+    Returns (y, intermediates) where intermediates holds counts/offsets/perm and the
+    per-row h and FC2 outputs in permuted order (float64).
+    """
+    X = np.asarray(x, dtype=np.float64)
+    ids = np.asarray(ids)
+    T, k = ids.shape
+    E = len(w13)
+    counts, offsets, perm_src, perm_inv = permute(ids, E)
+    x_perm = X[perm_src // k]
+    I = np.asarray(w2[0]).shape[1]
+    h = np.zeros((T * k, I))
+    out = np.zeros((T * k, X.shape[1]))
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        if a == b:
+            continue
+        w13e = np.asarray(w13[e], dtype=np.float64)
+        w2e = np.asarray(w2[e], dtype=np.float64)
+        h[a:b] = swiglu(x_perm[a:b] @ w13e.T, I)
+        out[a:b] = h[a:b] @ w2e.T
+    sc = np.asarray(scales, dtype=np.float64).reshape(-1)
+    y = np.zeros_like(X)
+    for j in range(k):
+        f = np.arange(T) * k + j
+        y += sc[f][:, None] * out[perm_inv[f]]
+    if w13_s is not None:
+        y += expert_ffn(X, w13_s, w2_s)
+    inter = dict(counts=counts, offsets=offsets, perm_src=perm_src, perm_inv=perm_inv,
+                 h=h, out=out)
+    return y, inter

@@ -1,0 +1,75 @@
+"""The pins must catch plausible mistakes: each test plants one in the oracle (on the
+CPU, through monkeypatch) and checks that a pin then fails."""
+import numpy as np
+import pytest
+
+import oracle
+import oracle.moe_oracle as om
+import tests.test_oracle_pins as pins
+
+
+def _fails(fn, *args):
+    with pytest.raises(AssertionError):
+        fn(*args)
+
+
+def test_swapped_gate_up_is_caught(monkeypatch, golden_dir):
+    def bad_swiglu(a, I):
+        g, u = a[:, I:2 * I], a[:, :I]
+        return g / (1.0 + np.exp(-g)) * u
+    monkeypatch.setattr(om, "swiglu", bad_swiglu)
+    _fails(pins.test_golden_ffn_and_layer, golden_dir)
+
+
+def test_biased_weights_are_caught(monkeypatch, golden_dir):
+    real = om.deepseek_keys
+
+    def bad_keys(l, b):
+        s64, kappa = real(l, b)
+        return kappa.astype(np.float64), kappa   # weights would then use biased scores
+    monkeypatch.setattr(om, "deepseek_keys", bad_keys)
+    _fails(pins.test_golden_grouped_deepseek, golden_dir)
+
+
+def test_full_group_sum_is_caught(monkeypatch, golden_dir):
+    def bad_group_select(kappa, n_group, topk_group):
+        T, E = kappa.shape
+        gscore = kappa.reshape(T, n_group, E // n_group).sum(-1).astype(np.float32)
+        return om.topk_desc(gscore, topk_group), gscore
+    monkeypatch.setattr(om, "group_select", bad_group_select)
+    _fails(pins.test_golden_grouped_deepseek, golden_dir)
+
+
+def test_highest_index_tiebreak_is_caught(monkeypatch):
+    def bad_topk(keys, k):
+        rev = keys[..., ::-1]
+        idx = np.argsort(-rev, axis=-1, kind="stable")[..., :k]
+        return keys.shape[-1] - 1 - idx
+    monkeypatch.setattr(om, "topk_desc", bad_topk)
+    _fails(pins.test_topk_matches_rank_counting, oracle.RENORMALIZE)
+
+
+def test_default_with_renorm_is_caught(monkeypatch):
+    real = om.route
+
+    def bad_route(logits, method, top_k, *a, **kw):
+        if method == om.DEFAULT:
+            method = om.RENORMALIZE_NAIVE
+        return real(logits, method, top_k, *a, **kw)
+    monkeypatch.setattr(om, "route", bad_route)
+    monkeypatch.setattr(oracle, "route", bad_route)
+    _fails(pins.test_weights_closed_forms)
+
+
+def test_unstable_permute_is_caught(monkeypatch):
+    def bad_permute(ids, E):
+        flat = np.asarray(ids, dtype=np.int64).reshape(-1)
+        counts = np.bincount(flat, minlength=E)[:E]
+        offsets = np.concatenate([[0], np.cumsum(counts)])
+        perm_src = np.lexsort((-np.arange(flat.size), flat))  # descending f inside a block
+        perm_inv = np.empty_like(perm_src)
+        perm_inv[perm_src] = np.arange(flat.size)
+        return counts, offsets, perm_src, perm_inv
+    monkeypatch.setattr(om, "permute", bad_permute)
+    monkeypatch.setattr(oracle, "permute", bad_permute)
+    _fails(pins.test_permute_brute_force_and_identity)
