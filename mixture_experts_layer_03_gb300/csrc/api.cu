@@ -1,0 +1,279 @@
+// C ABI entry points: argument validation on the host, workspace layout, and the
+// launch sequence of the forward. Nothing here allocates device memory.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+thread_local char g_err[512] = {0};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int32_t problem_reason(const moe_problem& p) {
+  if (p.T < 0 || p.T > (int64_t{1} << 24)) return MOE_REASON_T_RANGE;
+  if (p.E < 1 || p.E > 256) return MOE_REASON_E_RANGE;
+  if (p.k < 1 || p.k > 8) return MOE_REASON_TOPK_RANGE;
+  if (p.H < 64 || p.H % 64 != 0 || p.H > 32768) return MOE_REASON_H_ALIGN;
+  if (p.I < 64 || p.I % 64 != 0 || p.I > 65536) return MOE_REASON_I_ALIGN;
+  if (p.shared_I < 0 || p.shared_I % 64 != 0 || p.shared_I > 65536) return MOE_REASON_SHARED_I_ALIGN;
+  const int64_t rows = p.T * p.k + (p.shared_I > 0 ? p.T : 0);
+  if (rows >= (int64_t{1} << 31)) return MOE_REASON_ROWS;
+  return MOE_REASON_OK;
+}
+
+int32_t route_reason(int64_t T, const moe_route_params& r) {
+  if (T < 0 || T > (int64_t{1} << 31) / 8) return MOE_REASON_T_RANGE;
+  if (r.num_experts < 1 || r.num_experts > 256) return MOE_REASON_E_RANGE;
+  if (r.top_k < 1 || r.top_k > 8 || r.top_k > r.num_experts) return MOE_REASON_TOPK_RANGE;
+  switch (r.method) {
+    case MOE_ROUTE_DEFAULT:
+    case MOE_ROUTE_RENORMALIZE:
+    case MOE_ROUTE_RENORMALIZE_NAIVE:
+    case MOE_ROUTE_SIGMOID_RENORM:
+      return MOE_REASON_OK;
+    case MOE_ROUTE_DEEPSEEKV3: {
+      // Fused-routing limits of the TensorRT-LLM MoE page, section "融合算子与回退阈值":
+      // top_k <= 8, E <= 256, experts per group <= 32, experts per group * topk_group <= 256.
+      if (r.n_group < 1 || r.n_group > 32 || r.num_experts % r.n_group != 0) return MOE_REASON_GROUPS;
+      const int epg = r.num_experts / r.n_group;
+      if (epg < 2 || epg > 32) return MOE_REASON_GROUPS;
+      if (r.topk_group < 1 || r.topk_group > r.n_group) return MOE_REASON_GROUPS;
+      if (epg * r.topk_group > 256 || r.top_k > epg * r.topk_group) return MOE_REASON_GROUPS;
+      return MOE_REASON_OK;
+    }
+    default:
+      return MOE_REASON_METHOD;
+  }
+}
+
+int g_sm_count[64] = {0};
+
+}  // namespace
+
+moe_status set_error(moe_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+bool compute_layout(const moe_problem& p, moe_ws_layout* out) {
+  if (problem_reason(p) != MOE_REASON_OK) return false;
+  moe_ws_layout L;
+  memset(&L, 0, sizeof(L));
+  const int64_t P = p.T * p.k;
+  const int G = p.E + (p.shared_I > 0 ? 1 : 0);
+  const int nb = static_cast<int>((P + kPermChunk - 1) / kPermChunk);
+  const int Ih = p.shared_I > p.I ? p.shared_I : p.I;
+  const int64_t R = P + (p.shared_I > 0 ? p.T : 0);
+  const size_t A = 1024;
+  size_t o = 0;
+  L.status = o;      o = align_up(o + 16, A);
+  L.counts = o;      o = align_up(o + 4 * size_t(G), A);
+  L.starts = o;      o = align_up(o + 4 * size_t(G), A);
+  L.offsets = o;     o = align_up(o + 4 * size_t(p.E + 1), A);
+  L.tile_off1 = o;   o = align_up(o + 4 * size_t(G + 1), A);
+  L.tile_off2 = o;   o = align_up(o + 4 * size_t(G + 1), A);
+  L.block_hist = o;  o = align_up(o + 4 * size_t(nb) * size_t(p.E), A);
+  L.perm_src = o;    o = align_up(o + 4 * size_t(P), A);
+  L.perm_inv = o;    o = align_up(o + 4 * size_t(P), A);
+  L.x_perm = o;      o = align_up(o + 2 * size_t(R) * size_t(p.H), A);
+  L.h = o;           o = align_up(o + 2 * size_t(R) * size_t(Ih), A);
+  L.out_perm = o;    o = align_up(o + 2 * size_t(R) * size_t(p.H), A);
+  L.total = o;
+  L.rows = R;
+  L.groups = G;
+  L.n_chunks = nb;
+  L.h_ld = Ih;
+  *out = L;
+  return true;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+moe_status check_forward_common(const moe_problem* p, void* workspace, size_t ws_bytes,
+                                moe_ws_layout* L) {
+  if (!p) return set_error(MOE_ERR_INVALID_ARG, "problem is NULL");
+  const int32_t reason = problem_reason(*p);
+  if (reason != MOE_REASON_OK)
+    return set_error(MOE_ERR_UNSUPPORTED, "problem outside the supported envelope (reason %d)", reason);
+  compute_layout(*p, L);
+  if (p->T == 0) return MOE_OK;
+  if (!workspace) return set_error(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 1023u) != 0)
+    return set_error(MOE_ERR_INVALID_ARG, "workspace must be 1024-byte aligned");
+  if (ws_bytes < L->total)
+    return set_error(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", ws_bytes, L->total);
+  return MOE_OK;
+}
+
+bool shared_args_ok(const moe_problem* p, const void* a, const void* b) {
+  if (p->shared_I > 0) return a && b && aligned16(a) && aligned16(b);
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported problem";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_BAD_ID: return "device saw an expert id outside [0, E)";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
+    case MOE_ERR_NOT_IMPLEMENTED: return "not implemented";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error(void) { return g_err; }
+
+moe_status moe_can_implement(const moe_problem* p, int32_t* reason) {
+  if (!p) {
+    if (reason) *reason = MOE_REASON_OK;
+    return MOE_ERR_INVALID_ARG;
+  }
+  const int32_t r = problem_reason(*p);
+  if (reason) *reason = r;
+  return r == MOE_REASON_OK ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+size_t moe_workspace_bytes(const moe_problem* p) {
+  moe_ws_layout L;
+  if (!p || !compute_layout(*p, &L)) return 0;
+  return L.total;
+}
+
+moe_status moe_workspace_layout(const moe_problem* p, moe_ws_layout* out) {
+  if (!p || !out) return set_error(MOE_ERR_INVALID_ARG, "NULL argument");
+  if (!compute_layout(*p, out)) return set_error(MOE_ERR_UNSUPPORTED, "problem outside the envelope");
+  return MOE_OK;
+}
+
+moe_status moe_route(const float* logits, int64_t T, const float* bias, const moe_route_params* p,
+                     int32_t* ids, float* scales, void* stream) {
+  if (!p) return set_error(MOE_ERR_INVALID_ARG, "route params are NULL");
+  const int32_t r = route_reason(T, *p);
+  if (r != MOE_REASON_OK) return set_error(MOE_ERR_UNSUPPORTED, "routing outside the envelope (reason %d)", r);
+  if (T == 0) return MOE_OK;
+  if (!logits || !ids || !scales) return set_error(MOE_ERR_INVALID_ARG, "NULL logits/ids/scales");
+  if (!aligned16(logits) || !aligned16(ids) || !aligned16(scales) || (bias && !aligned16(bias)))
+    return set_error(MOE_ERR_INVALID_ARG, "route pointers must be 16-byte aligned");
+  return launch_route(logits, T, bias, *p, ids, scales, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_permute(const moe_problem* p, const void* x, const int32_t* ids, void* workspace,
+                       size_t ws_bytes, void* stream) {
+  moe_ws_layout L;
+  moe_status st = check_forward_common(p, workspace, ws_bytes, &L);
+  if (st != MOE_OK || p->T == 0) return st;
+  if (!x || !ids || !aligned16(x) || !aligned16(ids))
+    return set_error(MOE_ERR_INVALID_ARG, "x/ids NULL or not 16-byte aligned");
+  return launch_permute(*p, L, x, ids, static_cast<char*>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_fc1(const moe_problem* p, const void* w13, const void* w13_s, void* workspace,
+                   size_t ws_bytes, void* stream) {
+  moe_ws_layout L;
+  moe_status st = check_forward_common(p, workspace, ws_bytes, &L);
+  if (st != MOE_OK || p->T == 0) return st;
+  if (!w13 || !aligned16(w13) || !shared_args_ok(p, w13_s, w13_s))
+    return set_error(MOE_ERR_INVALID_ARG, "w13/w13_s NULL or not 16-byte aligned");
+  return launch_fc1(*p, L, w13, w13_s, static_cast<char*>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_fc2(const moe_problem* p, const void* w2, const void* w2_s, void* workspace,
+                   size_t ws_bytes, void* stream) {
+  moe_ws_layout L;
+  moe_status st = check_forward_common(p, workspace, ws_bytes, &L);
+  if (st != MOE_OK || p->T == 0) return st;
+  if (!w2 || !aligned16(w2) || !shared_args_ok(p, w2_s, w2_s))
+    return set_error(MOE_ERR_INVALID_ARG, "w2/w2_s NULL or not 16-byte aligned");
+  return launch_fc2(*p, L, w2, w2_s, static_cast<char*>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_finalize(const moe_problem* p, const float* scales, void* y, void* workspace,
+                        size_t ws_bytes, void* stream) {
+  moe_ws_layout L;
+  moe_status st = check_forward_common(p, workspace, ws_bytes, &L);
+  if (st != MOE_OK || p->T == 0) return st;
+  if (!scales || !y || !aligned16(scales) || !aligned16(y))
+    return set_error(MOE_ERR_INVALID_ARG, "scales/y NULL or not 16-byte aligned");
+  return launch_finalize(*p, L, scales, y, static_cast<const char*>(workspace),
+                         static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward(const moe_problem* p, const void* x, const int32_t* ids, const float* scales,
+                       const void* w13, const void* w2, const void* w13_s, const void* w2_s, void* y,
+                       void* workspace, size_t ws_bytes, void* stream) {
+  moe_ws_layout L;
+  moe_status st = check_forward_common(p, workspace, ws_bytes, &L);
+  if (st != MOE_OK || p->T == 0) return st;
+  if (!x || !ids || !scales || !w13 || !w2 || !y)
+    return set_error(MOE_ERR_INVALID_ARG, "NULL tensor argument");
+  if (!aligned16(x) || !aligned16(ids) || !aligned16(scales) || !aligned16(w13) || !aligned16(w2) ||
+      !aligned16(y))
+    return set_error(MOE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (!shared_args_ok(p, w13_s, w2_s))
+    return set_error(MOE_ERR_INVALID_ARG, "shared expert weights NULL or not 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  if ((st = launch_permute(*p, L, x, ids, ws, s)) != MOE_OK) return st;
+  if ((st = launch_fc1(*p, L, w13, w13_s, ws, s)) != MOE_OK) return st;
+  if ((st = launch_fc2(*p, L, w2, w2_s, ws, s)) != MOE_OK) return st;
+  return launch_finalize(*p, L, scales, y, ws, s);
+}
+
+moe_status moe_read_device_status(void* workspace, void* stream, int32_t* flags) {
+  if (!workspace) return set_error(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(v), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (flags) *flags = v;
+  if (v & MOE_DEVICE_FLAG_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
+  if (v & MOE_DEVICE_FLAG_BAD_ID) return MOE_ERR_DEVICE_BAD_ID;
+  return MOE_OK;
+}
+
+moe_status moe_cast_f32_to_bf16(const float* in, void* out, int64_t n, void* stream) {
+  if (n < 0) return set_error(MOE_ERR_INVALID_ARG, "negative length");
+  if (n == 0) return MOE_OK;
+  if (!in || !out) return set_error(MOE_ERR_INVALID_ARG, "NULL pointer");
+  return launch_cast_f32_bf16(in, out, n, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// Declarations shared by the translation units of the library (not public).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Permute: one block handles a chunk of this many (token, slot) pairs.
+constexpr int kPermChunk = 4096;
+constexpr int kPermThreads = 512;
+
+// Grouped GEMM tiling.
+constexpr int kTileRows = 128;    // token rows of a full (token-major) tile
+constexpr int kFc1Cols = 128;     // FC1 output channels per tile (gate and up each)
+constexpr int kFc2Cols = 256;     // FC2 output channels per tile
+
+// Fills the layout; returns false when the problem is outside the envelope.
+bool compute_layout(const moe_problem& p, moe_ws_layout* out);
+
+// Records a message for moe_last_error() and returns the status.
+moe_status set_error(moe_status s, const char* fmt, ...);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+// ---- launchers (each returns MOE_OK or MOE_ERR_CUDA; arguments already validated)
+
+moe_status launch_route(const float* logits, int64_t T, const float* bias,
+                        const moe_route_params& p, int32_t* ids, float* scales,
+                        cudaStream_t s);
+
+moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const void* x,
+                          const int32_t* ids, char* ws, cudaStream_t s);
+
+moe_status launch_fc1(const moe_problem& p, const moe_ws_layout& L, const void* w13,
+                      const void* w13_s, char* ws, cudaStream_t s);
+
+moe_status launch_fc2(const moe_problem& p, const moe_ws_layout& L, const void* w2,
+                      const void* w2_s, char* ws, cudaStream_t s);
+
+moe_status launch_finalize(const moe_problem& p, const moe_ws_layout& L, const float* scales,
+                           void* y, const char* ws, cudaStream_t s);
+
+moe_status launch_cast_f32_bf16(const float* in, void* out, int64_t n, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,256 @@
+// Step 2: permute (Dense GEMM -> GroupedGEMM article, sections 2.1-2.2: rows of each
+// expert gathered into one contiguous block; blocks concatenated in expert order and
+// described by an offset array; one grouped launch then covers every expert).
+//
+// Deterministic, no atomics in the ordering:
+//   hist_kernel    per chunk of kPermChunk (token, slot) pairs: histogram over experts
+//   plan_kernel    every chunk: column sums + exclusive scan of the histograms give each
+//                  (chunk, expert) its base row; inside the chunk, ranks come from
+//                  warp match_any and a running per-expert count, so rows of an expert
+//                  keep ascending flat index f = t*k + j. Chunk 0 also writes counts,
+//                  starts, offsets and the FC1/FC2 tile lists.
+//   gather_kernel  x_perm[r] = x[perm_src[r] / k] (and x[t] for the shared rows),
+//                  16-byte vector copies, one warp per row.
+#include <cstdint>
+
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kPermWarps = kPermThreads / 32;
+
+__global__ void __launch_bounds__(kPermThreads)
+hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int32_t* __restrict__ block_hist) {
+  __shared__ int32_t h[256];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+  __syncthreads();
+  const int64_t f0 = static_cast<int64_t>(blockIdx.x) * kPermChunk;
+  const int64_t f1 = (P < f0 + kPermChunk ? P : f0 + kPermChunk);
+  for (int64_t f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
+    const int e = ids[f];
+    if (e >= 0 && e < E) atomicAdd(&h[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) block_hist[blockIdx.x * E + e] = h[e];
+}
+
+// Block-wide exclusive scan of v over the first n <= kPermThreads threads.
+// Returns the exclusive prefix; *total receives the sum.
+__device__ int block_exclusive_scan(int v, int n, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (static_cast<int>(threadIdx.x) >= n) v = 0;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kPermWarps ? s_warp[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += o;
+    }
+    if (lane < kPermWarps) s_warp[lane] = wi - w;   // exclusive warp prefix
+    if (lane == kPermWarps - 1) s_warp[kPermWarps] = wi;
+  }
+  __syncthreads();
+  const int res = s_warp[warp] + incl - v;
+  *total = s_warp[kPermWarps];
+  __syncthreads();
+  return res;
+}
+
+struct PlanArgs {
+  const int32_t* ids;
+  int64_t P;
+  int T;
+  int E;
+  int k;
+  int nb;
+  int has_shared;
+  int I;
+  int shared_I;
+  int H;
+  const int32_t* block_hist;
+  int32_t* counts;     // [G]
+  int32_t* starts;     // [G]
+  int32_t* offsets;    // [E+1]
+  int32_t* tile_off1;  // [G+1]
+  int32_t* tile_off2;  // [G+1]
+  int32_t* perm_src;   // [P]
+  int32_t* perm_inv;   // [P]
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
+  __shared__ int32_t s_run[256];                // next free row per expert in this chunk
+  __shared__ int32_t s_wcnt[kPermWarps][256];   // rows per (warp, expert) in a sub-chunk
+  __shared__ int s_warp[kPermWarps + 1];
+  const int tid = threadIdx.x;
+  const int b = blockIdx.x;
+  const int E = a.E;
+
+  // Column sums and this chunk's prefix over earlier chunks.
+  int tot = 0, before = 0;
+  if (tid < E) {
+    for (int c = 0; c < a.nb; ++c) {
+      const int v = a.block_hist[c * E + tid];
+      if (c < b) before += v;
+      tot += v;
+    }
+  }
+  int p_valid = 0;
+  const int off = block_exclusive_scan(tot, E, s_warp, &p_valid);
+  if (tid < E) s_run[tid] = off + before;
+  for (int i = tid; i < kPermWarps * 256; i += blockDim.x) (&s_wcnt[0][0])[i] = 0;
+
+  if (b == 0) {
+    // Group table: routed experts 0..E-1, then the shared expert (all T tokens, rows
+    // starting at P). Tiles per group: full 128-row tiles plus one remainder tile, times
+    // the output-channel tiles of the GEMM.
+    const int G = E + a.has_shared;
+    int cnt = 0, start = 0, n1 = 0, n2 = 0;
+    if (tid < E) {
+      cnt = tot;
+      start = off;
+      a.offsets[tid] = off;
+    } else if (tid == E && a.has_shared) {
+      cnt = a.T;
+      start = static_cast<int>(a.P);
+    }
+    if (tid == E) a.offsets[E] = p_valid;
+    if (tid < G) {
+      a.counts[tid] = cnt;
+      a.starts[tid] = start;
+      const int mt = cnt / kTileRows + (cnt % kTileRows != 0);
+      const int nI = (tid < E) ? a.I : a.shared_I;
+      n1 = mt * ((nI + kFc1Cols - 1) / kFc1Cols);
+      n2 = mt * ((a.H + kFc2Cols - 1) / kFc2Cols);
+    }
+    int tot1 = 0, tot2 = 0;
+    const int o1 = block_exclusive_scan(n1, G, s_warp, &tot1);
+    const int o2 = block_exclusive_scan(n2, G, s_warp, &tot2);
+    if (tid < G) {
+      a.tile_off1[tid] = o1;
+      a.tile_off2[tid] = o2;
+    }
+    if (tid == 0) {
+      a.tile_off1[G] = tot1;
+      a.tile_off2[G] = tot2;
+    }
+  }
+  __syncthreads();
+
+  // Stable ranks inside the chunk, kPermThreads pairs at a time.
+  const int lane = tid & 31, warp = tid >> 5;
+  const int64_t f0 = static_cast<int64_t>(b) * kPermChunk;
+  const int64_t f1 = (a.P < f0 + kPermChunk ? a.P : f0 + kPermChunk);
+  for (int64_t base = f0; base < f1; base += kPermThreads) {
+    const int64_t f = base + tid;
+    int e = -1;
+    if (f < f1) {
+      e = a.ids[f];
+      if (e < 0 || e >= E) {
+        a.perm_inv[f] = -1;
+        atomicOr(a.status, MOE_DEVICE_FLAG_BAD_ID);
+        e = -1;
+      }
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+    const bool leader = rank_in_warp == 0;
+    if (e >= 0 && leader) s_wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int pos = s_run[e] + rank_in_warp;
+      for (int w = 0; w < warp; ++w) pos += s_wcnt[w][e];
+      a.perm_src[pos] = static_cast<int32_t>(f);
+      a.perm_inv[f] = pos;
+    }
+    __syncthreads();
+    if (tid < E) {
+      int add = 0;
+      for (int w = 0; w < kPermWarps; ++w) {
+        add += s_wcnt[w][tid];
+        s_wcnt[w][tid] = 0;
+      }
+      s_run[tid] += add;
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(256)
+gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ perm_src,
+              const int32_t* __restrict__ offsets, int64_t P, int E, int k, int64_t rows,
+              int H, __nv_bfloat16* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t p_valid = offsets[E];
+  const int nvec = H / 8;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       r < rows; r += warps) {
+    int64_t src;
+    if (r < P) {
+      if (r >= p_valid) continue;
+      src = perm_src[r] / k;
+    } else {
+      src = r - P;
+    }
+    const uint4* s = reinterpret_cast<const uint4*>(x + src * H);
+    uint4* d = reinterpret_cast<uint4*>(x_perm + r * H);
+    for (int v = lane; v < nvec; v += 32) d[v] = __ldg(s + v);
+  }
+}
+
+}  // namespace
+
+moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const void* x,
+                          const int32_t* ids, char* ws, cudaStream_t s) {
+  const int64_t P = p.T * p.k;
+  cudaError_t err = cudaMemsetAsync(ws + L.status, 0, 16, s);
+  if (err != cudaSuccess) return set_error(MOE_ERR_CUDA, "status clear: %s", cudaGetErrorString(err));
+  const int nb = L.n_chunks;
+  hist_kernel<<<nb, kPermThreads, 0, s>>>(ids, P, p.E, reinterpret_cast<int32_t*>(ws + L.block_hist));
+  PlanArgs a;
+  a.ids = ids;
+  a.P = P;
+  a.T = static_cast<int>(p.T);
+  a.E = p.E;
+  a.k = p.k;
+  a.nb = nb;
+  a.has_shared = p.shared_I > 0;
+  a.I = p.I;
+  a.shared_I = p.shared_I;
+  a.H = p.H;
+  a.block_hist = reinterpret_cast<const int32_t*>(ws + L.block_hist);
+  a.counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  a.starts = reinterpret_cast<int32_t*>(ws + L.starts);
+  a.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  a.tile_off1 = reinterpret_cast<int32_t*>(ws + L.tile_off1);
+  a.tile_off2 = reinterpret_cast<int32_t*>(ws + L.tile_off2);
+  a.perm_src = reinterpret_cast<int32_t*>(ws + L.perm_src);
+  a.perm_inv = reinterpret_cast<int32_t*>(ws + L.perm_inv);
+  a.status = reinterpret_cast<int32_t*>(ws + L.status);
+  plan_kernel<<<nb, kPermThreads, 0, s>>>(a);
+  const int sms = device_sm_count();
+  const int64_t rows = L.rows;
+  int64_t blocks = (rows + 7) / 8;
+  if (blocks > static_cast<int64_t>(sms) * 16) blocks = static_cast<int64_t>(sms) * 16;
+  gather_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(x), a.perm_src, a.offsets, P, p.E, p.k, rows, p.H,
+      reinterpret_cast<__nv_bfloat16*>(ws + L.x_perm));
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return set_error(MOE_ERR_CUDA, "permute launch: %s", cudaGetErrorString(err));
+  return MOE_OK;
+}
+
+}  // namespace moe

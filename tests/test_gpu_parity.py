@@ -1,0 +1,331 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the CPU oracle on the same
+seeded inputs. Expert ids, counts, offsets and the permutation must match bit for bit;
+routing scales within 1e-6 relative; h / FC2 rows / y within max|err| <= tol * max|ref|
+(y: 2e-2, the bf16 output tolerance; the oracle accumulates in fp64)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import (WORKLOADS, Workload, make_inputs, DEFAULT, RENORMALIZE, DEEPSEEKV3,
+                       RENORMALIZE_NAIVE, SIGMOID_RENORM)
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+Y_TOL = 2e-2
+H_TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import mixture_experts_layer_03_gb300 as m
+    return m
+
+
+class ExpertView:
+    """Per-expert host float64 copies of a device weight tensor (one expert at a time)."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __len__(self):
+        return self.t.shape[0]
+
+    def __getitem__(self, e):
+        return self.t[int(e)].cpu().double().numpy()
+
+
+def _np64(t):
+    return t.cpu().double().numpy()
+
+
+def _check_close(got, ref, tol, what):
+    got = np.asarray(got, np.float64)
+    err = np.abs(got - ref).max() if ref.size else 0.0
+    bound = tol * (np.abs(ref).max() if ref.size else 0.0)
+    assert err <= bound, f"{what}: max|err| = {err:.4e} > {bound:.4e}"
+    return err, bound
+
+
+def _to_bf16_dev(moe, t, dev="cuda"):
+    t = t.to(dev)
+    return moe.moe_cast_f32_to_bf16(t) if t.dtype == torch.float32 else t
+
+
+# ------------------------------------------------------------------------ routing
+
+ROUTE_CASES = [
+    # (T, E, k, method, n_group, topk_group, rsf, logit_scale, int_logits)
+    (257, 8, 2, RENORMALIZE_NAIVE, 1, 1, 1.0, 1.0, False),
+    (100, 8, 2, DEFAULT, 1, 1, 1.0, 1.0, False),
+    (100, 64, 6, RENORMALIZE, 1, 1, 1.0, 3.0, False),
+    (100, 128, 8, SIGMOID_RENORM, 1, 1, 1.0, 1.0, False),
+    (100, 256, 8, DEEPSEEKV3, 8, 4, 2.5, 1.0, False),
+    (100, 96, 5, DEEPSEEKV3, 4, 2, 1.0, 1.0, False),
+    (100, 33, 3, RENORMALIZE_NAIVE, 1, 1, 1.0, 1.0, False),   # E not a multiple of 32
+    (64, 16, 4, RENORMALIZE_NAIVE, 1, 1, 1.0, 1.0, True),     # many exact ties
+    (64, 16, 4, DEEPSEEKV3, 4, 2, 1.0, 1.0, True),            # ties in keys and group scores
+    (64, 1, 1, SIGMOID_RENORM, 1, 1, 1.0, 1.0, False),        # one expert
+    (64, 8, 8, DEFAULT, 1, 1, 1.0, 1.0, False),               # k = E
+    (1, 256, 8, RENORMALIZE, 1, 1, 1.0, 1.0, False),          # one token
+]
+
+
+@pytest.mark.parametrize("case", ROUTE_CASES, ids=lambda c: f"T{c[0]}E{c[1]}k{c[2]}m{c[3]}")
+def test_route_parity(moe, case):
+    T, E, k, method, ng, tg, rsf, scale, int_logits = case
+    g = torch.Generator().manual_seed(11)
+    if int_logits:
+        logits = torch.randint(-2, 3, (T, E), generator=g).float()
+    else:
+        logits = torch.randn(T, E, generator=g) * scale
+    bias = torch.randn(E, generator=g) * 0.1 if method == DEEPSEEKV3 else None
+    ids, sc = moe.moe_route(logits.cuda(), method, k, bias=None if bias is None else bias.cuda(),
+                            n_group=ng, topk_group=tg, routed_scaling_factor=rsf)
+    ids_ref, sc_ref = oracle.route(logits.numpy(), method, k,
+                                   bias=None if bias is None else bias.numpy(), n_group=ng,
+                                   topk_group=tg, routed_scaling_factor=rsf)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(sc.cpu().numpy(), sc_ref, rtol=1e-6, atol=0)
+
+
+def test_route_nonfinite_logits_never_beat_finite(moe):
+    logits = torch.randn(32, 16)
+    logits[:, 3] = float("nan")
+    logits[:, 5] = float("inf")
+    logits[:, 7] = -float("inf")
+    ids, _ = moe.moe_route(logits.cuda(), RENORMALIZE_NAIVE, 4)
+    ids_ref, _ = oracle.route(logits.numpy(), RENORMALIZE_NAIVE, 4)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert not np.isin(ids.cpu().numpy(), [3, 5, 7]).any()
+
+
+# ------------------------------------------------------------------------ permute
+
+@pytest.mark.parametrize("T,E,k", [(300, 8, 2), (5000, 64, 4), (1, 4, 1), (2048, 256, 8),
+                                   (9000, 3, 3)])
+def test_permute_parity(moe, T, E, k):
+    g = torch.Generator().manual_seed(T + E)
+    ids = torch.randint(0, E, (T, k), generator=g, dtype=torch.int32)
+    H = 128
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    p = moe.make_problem(T, H, 64, E, k)
+    ws = moe.alloc_workspace(p)
+    moe.moe_permute(p, x.cuda(), ids.cuda(), ws)
+    torch.cuda.synchronize()
+    counts, offsets, perm_src, perm_inv = oracle.permute(ids.numpy(), E)
+    P = T * k
+    assert np.array_equal(ws.region("counts", E, torch.int32).cpu().numpy(), counts)
+    assert np.array_equal(ws.region("offsets", E + 1, torch.int32).cpu().numpy(), offsets)
+    assert np.array_equal(ws.region("perm_src", P, torch.int32).cpu().numpy(), perm_src)
+    assert np.array_equal(ws.region("perm_inv", P, torch.int32).cpu().numpy(), perm_inv)
+    xp = ws.region("x_perm", P * H, torch.bfloat16).view(P, H).cpu()
+    assert torch.equal(xp, x[torch.from_numpy(perm_src).long() // k])
+    # tile lists: per group floor(m/128) + (m%128 > 0) row tiles x channel tiles
+    mt = counts // 128 + (counts % 128 > 0)
+    t1 = ws.region("tile_off1", E + 1, torch.int32).cpu().numpy()
+    t2 = ws.region("tile_off2", E + 1, torch.int32).cpu().numpy()
+    assert np.array_equal(t1, np.concatenate([[0], np.cumsum(mt * 1)]))
+    assert np.array_equal(t2, np.concatenate([[0], np.cumsum(mt * 1)]))
+    st, flags = moe.moe_read_device_status(ws)
+    assert st == moe.MOE_OK and flags == 0
+
+
+# ------------------------------------------------------------------------ forward (small)
+
+def _random_case(T, H, I, E, k, shared_I=0, seed=0, ids_mode="route", method=RENORMALIZE_NAIVE):
+    g = torch.Generator().manual_seed(seed)
+    logits = torch.randn(T, E, generator=g)
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    w13 = (torch.randn(E, 2 * I, H, generator=g) * H ** -0.5).to(torch.bfloat16)
+    w2 = (torch.randn(E, H, I, generator=g) * I ** -0.5).to(torch.bfloat16)
+    w13s = w2s = None
+    if shared_I:
+        w13s = (torch.randn(2 * shared_I, H, generator=g) * H ** -0.5).to(torch.bfloat16)
+        w2s = (torch.randn(H, shared_I, generator=g) * shared_I ** -0.5).to(torch.bfloat16)
+    if ids_mode == "route":
+        ids, sc = oracle.route(logits.numpy(), method, k)
+    elif ids_mode == "one_expert":
+        ids = np.zeros((T, k), np.int32)
+        for j in range(k):
+            ids[:, j] = j
+        sc = np.full((T, k), 1.0 / k)
+    elif ids_mode == "random_dup":
+        ids = torch.randint(0, E, (T, k), generator=g).numpy().astype(np.int32)
+        sc = torch.rand(T, k, generator=g).numpy().astype(np.float64)
+    else:
+        raise ValueError(ids_mode)
+    return dict(x=x, w13=w13, w2=w2, w13s=w13s, w2s=w2s, ids=ids.astype(np.int32),
+                sc=sc.astype(np.float32))
+
+
+def _run_forward_steps(moe, c):
+    T, H = c["x"].shape
+    E, twoI, _ = c["w13"].shape
+    k = c["ids"].shape[1]
+    sI = 0 if c["w13s"] is None else c["w13s"].shape[0] // 2
+    p = moe.make_problem(T, H, twoI // 2, E, k, sI)
+    ws = moe.alloc_workspace(p)
+    dev = {n: (None if v is None else (torch.from_numpy(v) if isinstance(v, np.ndarray) else v).cuda())
+           for n, v in c.items()}
+    y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    moe.moe_permute(p, dev["x"], dev["ids"], ws)
+    moe.moe_fc1(p, dev["w13"], dev["w13s"], ws)
+    moe.moe_fc2(p, dev["w2"], dev["w2s"], ws)
+    moe.moe_finalize(p, dev["sc"], y, ws)
+    torch.cuda.synchronize()
+    return p, ws, y, dev
+
+
+SMALL_CASES = [
+    # T, H, I, E, k, shared_I, ids_mode
+    (300, 256, 192, 8, 2, 0, "route"),         # weight-major tiles, ragged FC1 channel tile
+    (700, 384, 320, 4, 2, 0, "route"),         # token-major + remainder tiles, ragged FC2 tile
+    (1000, 256, 256, 8, 1, 0, "one_expert"),   # one expert holds every row (7 full tiles + 104)
+    (513, 128, 128, 8, 8, 0, "route"),         # k = E: every expert every token
+    (200, 192, 128, 16, 4, 128, "random_dup"), # repeated ids in a row, shared expert
+    (130, 128, 64, 1, 1, 0, "route"),          # E = 1, k = 1: the dense FFN (128 + 2 rows)
+    (1, 128, 128, 8, 2, 0, "route"),           # a single token
+    (64, 256, 128, 32, 4, 192, "route"),       # shared expert wider than the routed ones
+    (96, 128, 256, 8, 2, 64, "route"),         # shared expert narrower than the routed ones
+]
+
+
+@pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: "T{}H{}I{}E{}k{}s{}-{}".format(*c))
+def test_forward_steps_parity(moe, case):
+    T, H, I, E, k, sI, mode = case
+    c = _random_case(T, H, I, E, k, sI, seed=T + H, ids_mode=mode)
+    p, ws, y, dev = _run_forward_steps(moe, c)
+    x64 = _np64(c["x"])
+    w13 = _np64(c["w13"])
+    w2 = _np64(c["w2"])
+    w13s = None if c["w13s"] is None else _np64(c["w13s"])
+    w2s = None if c["w2s"] is None else _np64(c["w2s"])
+    y_ref, inter = oracle.forward_permuted(x64, c["ids"], c["sc"], w13, w2, w13s, w2s)
+    P = T * k
+    assert np.array_equal(ws.region("perm_src", P, torch.int32).cpu().numpy(), inter["perm_src"])
+    L = ws.layout
+    R, Ih = L["rows"], L["h_ld"]
+    h = ws.region("h", R * Ih, torch.bfloat16).view(R, Ih).cpu().double().numpy()
+    _check_close(h[:P, :I], inter["h"], H_TOL, "FC1+SwiGLU h")
+    out = ws.region("out_perm", R * H, torch.bfloat16).view(R, H).cpu().double().numpy()
+    _check_close(out[:P], inter["out"], Y_TOL, "FC2 rows")
+    if sI:
+        hs_ref = oracle.swiglu(x64 @ w13s.T, sI)
+        _check_close(h[P:, :sI], hs_ref, H_TOL, "shared FC1")
+        _check_close(out[P:], hs_ref @ w2s.T, Y_TOL, "shared FC2")
+    _check_close(y.cpu().double().numpy(), y_ref, Y_TOL, "y")
+    # moe_forward (one call) gives the same bytes as the four steps
+    y2 = moe.moe_forward(dev["x"], dev["ids"], dev["sc"], dev["w13"], dev["w2"], dev["w13s"],
+                         dev["w2s"], workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y2, y)
+
+
+def test_forward_is_deterministic(moe):
+    c = _random_case(2000, 256, 256, 16, 4, 0, seed=3)
+    _, ws, y1, dev = _run_forward_steps(moe, c)
+    perm1 = ws.region("perm_src", 8000, torch.int32).clone()
+    y2 = moe.moe_forward(dev["x"], dev["ids"], dev["sc"], dev["w13"], dev["w2"], workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    assert torch.equal(perm1, ws.region("perm_src", 8000, torch.int32))
+
+
+def test_bad_ids_are_skipped_and_flagged(moe):
+    c = _random_case(64, 128, 128, 8, 2, 0, seed=5, ids_mode="random_dup")
+    ids = c["ids"].copy()
+    ids[3, 1] = 8
+    ids[10, 0] = -1
+    c["ids"] = ids
+    p, ws, y, dev = _run_forward_steps(moe, c)
+    st, flags = moe.moe_read_device_status(ws)
+    assert st == moe.MOE_ERR_DEVICE_BAD_ID and flags & moe.MOE_DEVICE_FLAG_BAD_ID
+    assert moe.moe_read_device_status(ws)[0] == moe.MOE_OK   # the read cleared it
+    sc = c["sc"].copy()
+    sc[3, 1] = 0
+    sc[10, 0] = 0
+    ids_ok = np.where(ids < 0, 0, np.where(ids >= 8, 0, ids))
+    y_ref = oracle.forward(_np64(c["x"]), ids_ok, sc, _np64(c["w13"]), _np64(c["w2"]))
+    _check_close(y.cpu().double().numpy(), y_ref, Y_TOL, "y with skipped rows")
+    pinv = ws.region("perm_inv", 128, torch.int32).cpu().numpy()
+    assert pinv[3 * 2 + 1] == -1 and pinv[10 * 2 + 0] == -1
+
+
+def test_zero_tokens_is_a_noop(moe):
+    x = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty(0, 2, dtype=torch.int32, device="cuda")
+    sc = torch.empty(0, 2, dtype=torch.float32, device="cuda")
+    w13 = torch.zeros(4, 128, 128, dtype=torch.bfloat16, device="cuda")
+    w2 = torch.zeros(4, 128, 64, dtype=torch.bfloat16, device="cuda")
+    y = moe.moe_forward(x, ids, sc, w13, w2)
+    assert y.shape == (0, 128)
+    i, s = moe.moe_route(torch.empty(0, 8, device="cuda"), RENORMALIZE_NAIVE, 2)
+    assert i.shape == (0, 2)
+
+
+def test_cast_is_round_to_nearest_even(moe):
+    v = torch.randn(100003) * 10
+    v[:4] = torch.tensor([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -0.0, float("inf")])
+    got = moe.moe_cast_f32_to_bf16(v.cuda()).cpu()
+    assert torch.equal(got.view(torch.int16), v.to(torch.bfloat16).view(torch.int16))
+
+
+# ------------------------------------------------------------------------ full-size workloads
+
+SAMPLE_TOKENS = {"tiny": 64, "mixtral_prefill": 16, "qwen3_decode": 16, "dsv3_layer": 4,
+                 "skewed": 16}
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["tiny", "mixtral_prefill", "qwen3_decode", "dsv3_layer", "skewed"])
+def test_workload_full_size(moe, name):
+    """The five workloads at full size, in the launch configuration the bench times
+    (moe_route then moe_forward on one stream). Routing, counts and permutation are
+    checked on every token; y on sampled tokens (plus the edge tokens)."""
+    w: Workload = WORKLOADS[name]
+    inp = make_inputs(w, device="cuda", seed=0)
+    if w.in_dtype == "f32":
+        x = moe.moe_cast_f32_to_bf16(inp["x"])
+        w13 = moe.moe_cast_f32_to_bf16(inp["w13"])
+        w2 = moe.moe_cast_f32_to_bf16(inp["w2"])
+    else:
+        x, w13, w2 = inp["x"], inp["w13"], inp["w2"]
+    w13s, w2s = inp["w13_s"], inp["w2_s"]
+    p = moe.make_problem(w.T, w.H, w.I, w.E, w.k, w.shared_I)
+    ws = moe.alloc_workspace(p)
+    ids, sc = moe.moe_route(inp["logits"], w.method, w.k, bias=inp["bias"], n_group=w.n_group,
+                            topk_group=w.topk_group, routed_scaling_factor=w.rsf)
+    y = moe.moe_forward(x, ids, sc, w13, w2, w13s, w2s, workspace=ws)
+    torch.cuda.synchronize()
+
+    logits = inp["logits"].cpu().numpy()
+    bias = None if inp["bias"] is None else inp["bias"].cpu().numpy()
+    ids_ref, sc_ref = oracle.route(logits, w.method, w.k, bias=bias, n_group=w.n_group,
+                                   topk_group=w.topk_group, routed_scaling_factor=w.rsf)
+    ids_gpu = ids.cpu().numpy()
+    mism = np.argwhere((ids_gpu != ids_ref).any(1)).ravel()
+    assert mism.size == 0, f"{name}: ids differ on tokens {mism[:10]}"
+    np.testing.assert_allclose(sc.cpu().numpy(), sc_ref, rtol=1e-6, atol=0)
+    counts, offsets, perm_src, perm_inv = oracle.permute(ids_ref, w.E)
+    assert np.array_equal(ws.region("counts", w.E, torch.int32).cpu().numpy(), counts)
+    assert np.array_equal(ws.region("perm_src", w.P, torch.int32).cpu().numpy(), perm_src)
+    assert np.array_equal(ws.region("perm_inv", w.P, torch.int32).cpu().numpy(), perm_inv)
+
+    rng = np.random.default_rng(0)
+    n = min(SAMPLE_TOKENS[name], w.T)
+    sample = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, n, replace=False)]))
+    if w.in_dtype == "f32":   # the oracle takes the fp32 originals (the cast counts as error)
+        xs = inp["x"][sample].cpu().double().numpy()
+        W13, W2 = ExpertView(inp["w13"]), ExpertView(inp["w2"])
+    else:
+        xs = x[sample].cpu().double().numpy()
+        W13, W2 = ExpertView(w13), ExpertView(w2)
+    W13s = None if w13s is None else _np64(w13s)
+    W2s = None if w2s is None else _np64(w2s)
+    y_ref = oracle.forward(xs, ids_ref[sample], sc_ref[sample], W13, W2, W13s, W2s)
+    _check_close(y[sample].cpu().double().numpy(), y_ref, Y_TOL, f"{name} y (sampled)")
+    assert torch.isfinite(y.float()).all()
+    st, flags = moe.moe_read_device_status(ws)
+    assert st == moe.MOE_OK and flags == 0
