@@ -1,0 +1,414 @@
+"""Benchmark of the MoE layer forward on GB300: tokens/s and % of roofline.
+
+One step = the whole hot path on one batch: moe_route (router logits -> ids, scales)
+then moe_forward (permute, FC1+SwiGLU, FC2, finalize), inputs resident in HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0). Under torchrun with N > 1 every rank runs its own
+replica of the workload (tokens are independent: no data-path collective) and the
+job value is the tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+if "OPENBLAS_NUM_THREADS" not in os.environ:   # the CPU oracle uses every host core
+    os.environ["OPENBLAS_NUM_THREADS"] = str(os.cpu_count() or 1)
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, Workload, make_inputs, flops, min_bytes  # noqa: E402
+
+METRIC = "MoE layer tokens/sec at 1 GB300 and % of roofline (HBM or bf16 TC)"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "mixtral_prefill"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.out.flush()
+        try:
+            lines = open(self.out.name).read().strip().splitlines()
+        except OSError:
+            lines = []
+        finally:
+            try:
+                os.unlink(self.out.name)
+            except OSError:
+                pass
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def oracle_tokens_per_s(w: Workload, inp_host: dict, sample: int):
+    """Time the oracle (routing of the sample + the layer on it) on host cores."""
+    import oracle
+    rng = np.random.default_rng(1)
+    idx = np.sort(rng.choice(w.T, size=min(sample, w.T), replace=False))
+    logits = inp_host["logits"][idx]
+    bias = inp_host["bias"]
+    t0 = time.perf_counter()
+    ids, sc = oracle.route(logits, w.method, w.k, bias=bias, n_group=w.n_group,
+                           topk_group=w.topk_group, routed_scaling_factor=w.rsf)
+    oracle.forward(inp_host["x"][idx], ids, sc, inp_host["w13"], inp_host["w2"],
+                   inp_host["w13_s"], inp_host["w2_s"])
+    dt = time.perf_counter() - t0
+    return len(idx) / dt, dt, len(idx)
+
+
+def host_inputs(inp: dict) -> dict:
+    """Host fp32 numpy copies of the device inputs (the oracle widens them to fp64)."""
+    out = {}
+    for n, v in inp.items():
+        out[n] = None if v is None else v.float().cpu().numpy()
+    return out
+
+
+def cpu_baseline(w: Workload, inp_host: dict, target_s: float = 10.0):
+    """The oracle on a sample sized for ~target_s of CPU work (cost = a + b * tokens)."""
+    _, t1, n1 = oracle_tokens_per_s(w, inp_host, 8)
+    _, t2, n2 = oracle_tokens_per_s(w, inp_host, 32)
+    b = max((t2 - t1) / max(n2 - n1, 1), 1e-6)
+    a = max(t1 - b * n1, 0.0)
+    n = int(min(w.T, max(32, (target_s - a) / b)))
+    rate, dt, n = oracle_tokens_per_s(w, inp_host, n)
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": round(rate, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.T} tokens of {w.name} (routing + fp64 layer), {dt:.1f} s"}
+
+
+# --------------------------------------------------------------------------- our arm
+
+def traffic_record(kernel_file: str, workload: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    src = os.path.join(ROOT, "mixture_experts_layer_03_gb300", "csrc", kernel_file)
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if rec.get("source_sha256") != sha:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def run_ours(args, rank, world):
+    import mixture_experts_layer_03_gb300 as moe
+    w = WORKLOADS[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    inp = make_inputs(w, device=dev, seed=rank)
+    if w.in_dtype == "f32":
+        x = moe.moe_cast_f32_to_bf16(inp["x"])
+        w13 = moe.moe_cast_f32_to_bf16(inp["w13"])
+        w2 = moe.moe_cast_f32_to_bf16(inp["w2"])
+    else:
+        x, w13, w2 = inp["x"], inp["w13"], inp["w2"]
+    w13s, w2s = inp["w13_s"], inp["w2_s"]
+    logits, bias = inp["logits"], inp["bias"]
+    p = moe.make_problem(w.T, w.H, w.I, w.E, w.k, w.shared_I)
+    ws = moe.alloc_workspace(p, dev)
+    ids = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+    sc = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+    y = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    route_kw = dict(bias=bias, n_group=w.n_group, topk_group=w.topk_group,
+                    routed_scaling_factor=w.rsf, ids=ids, scales=sc)
+
+    def step(lg=logits, xx=x):
+        s = torch.cuda.current_stream()
+        moe.moe_route(lg, w.method, w.k, stream=s, **route_kw)
+        moe.moe_forward(xx, ids, sc, w13, w2, w13s, w2s, y=y, workspace=ws, stream=s)
+
+    launches_per_step = 1 + 3 + 1 + 1 + 1   # route; hist, plan, gather; fc1; fc2; finalize
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    counts = ws.region("counts", w.E, torch.int32).cpu().numpy()
+    n_active = int((counts > 0).sum())
+
+    # The step as one CUDA graph (every call above is stream-ordered and allocation-free).
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        step()   # one eager call on the capture stream before capturing
+        cap.synchronize()
+        with torch.cuda.graph(graph, stream=cap):
+            step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays, L2 flushed between steps outside the step events.
+    # A sleep kernel first lets the host queue the whole loop, so no step waits on the host.
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda._sleep(20_000_000)
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+        barrier()
+    clocks = clk.summary()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * w.T * args.steps / (total_ms / 1e3)
+
+    # ---- per-kernel durations: the same kernels through the step entry points, queued
+    # behind a sleep kernel so each event pair brackets device time only.
+    names = ["route", "permute", "fc1", "fc2", "finalize"]
+    reps = max(3, min(args.steps, 10))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(reps)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(20_000_000)
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        e = evs[i]
+        e[0].record(stream)
+        moe.moe_route(logits, w.method, w.k, stream=stream, **route_kw)
+        e[1].record(stream)
+        moe.moe_permute(p, x, ids, ws, stream=stream)
+        e[2].record(stream)
+        moe.moe_fc1(p, w13, w13s, ws, stream=stream)
+        e[3].record(stream)
+        moe.moe_fc2(p, w2, w2s, ws, stream=stream)
+        e[4].record(stream)
+        moe.moe_finalize(p, sc, y, ws, stream=stream)
+        e[5].record(stream)
+    torch.cuda.synchronize()
+    kern_ms = {n: statistics.median([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(reps)])
+               for j, n in enumerate(names)}
+
+    # ---- end to end through the public API, eager calls: pinned host inputs copied in,
+    # the result copied out, every step.
+    x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_h.copy_(x)
+    lg_h = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
+    lg_h.copy_(logits)
+    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    x_d, lg_d = torch.empty_like(x), torch.empty_like(logits)
+    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ee[i][0].record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        step(lg_d, x_d)
+        y_h.copy_(y, non_blocking=True)
+        ee[i][1].record(stream)
+    barrier()
+    e2e_total = sum(a.elapsed_time(b) for a, b in ee)
+    if world > 1:
+        t = torch.tensor([e2e_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e = {"value": round(world * w.T * args.steps / (e2e_total / 1e3), 1), "unit": UNIT,
+           "h2d_bytes_per_step": x.numel() * x.element_size() + logits.numel() * 4,
+           "d2h_bytes_per_step": y.numel() * y.element_size(),
+           "how": "eager moe_route + moe_forward calls, pinned host x/logits in and y out each step"}
+    st, flags = moe.moe_read_device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {st} flags {flags}")
+
+    # ---- roofline of the dominant kernel and of the whole layer
+    peaks, peak_src = load_peaks()
+    P_tc = peaks["bf16_tflops"]
+    fc1_flops = 2.0 * w.P * 2 * w.I * w.H + 2.0 * w.T * 2 * w.shared_I * w.H
+    fc1_bytes = (n_active * 2 * w.I * w.H + 2 * w.shared_I * w.H) * 2 + \
+        (w.P + (w.T if w.shared_I else 0)) * (w.H + w.I) * 2
+    fc1_t = kern_ms["fc1"] * 1e-3
+    tensor_bound = fc1_flops / (P_tc * 1e12) >= fc1_bytes / (peaks["hbm_gbs"] * 1e9)
+    if tensor_bound:
+        ach = fc1_flops / fc1_t / 1e12
+        roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": P_tc, "unit": "TFLOP/s",
+                    "frac": round(ach / P_tc, 4)}
+    else:
+        ach = fc1_bytes / fc1_t / 1e9
+        roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4)}
+    roofline.update({"traffic": traffic_record("grouped_gemm.cu", args.workload),
+                     "kernel": "grouped_gemm_kernel<FC1+SwiGLU>",
+                     "peak_source": f"{peak_src} ({'bf16_tflops burst' if tensor_bound else 'hbm_gbs'})",
+                     "algorithmic_flops_per_launch": fc1_flops,
+                     "algorithmic_bytes_per_launch": fc1_bytes, "ms_per_launch": round(kern_ms["fc1"], 4)})
+    fl = flops(w)
+    by = min_bytes(w, n_active)
+    t_tc, t_hbm = fl / (P_tc * 1e12), by / (peaks["hbm_gbs"] * 1e9)
+    t_roof = max(t_tc, t_hbm)
+    layer = {"bound": "tensor" if t_tc >= t_hbm else "hbm",
+             "t_roof_ms": round(t_roof * 1e3, 4), "t_ms": round(ms_per_step, 4),
+             "frac": round(t_roof * 1e3 / ms_per_step, 4), "flops": fl, "bytes": by,
+             "n_active_experts": n_active,
+             "achieved_tflops": round(fl / (ms_per_step * 1e-3) / 1e12, 1),
+             "achieved_gbs": round(by / (ms_per_step * 1e-3) / 1e9, 1),
+             "peaks": f"{peak_src}: hbm_gbs {peaks['hbm_gbs']}, bf16_tflops (burst) {P_tc}"}
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations/logits, N(0, fan_in^-1/2) random-init weights)",
+        "config": {"workload": w.describe(), "T": w.T, "H": w.H, "I": w.I, "E": w.E, "k": w.k,
+                   "routing_method": w.method, "shared_I": w.shared_I,
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write outside the step events)",
+                   "launch": "moe_route + moe_forward captured once as a CUDA graph, replayed per step",
+                   "parallelism": f"replicas x{world} (no collective on the data path)"},
+        "roofline": roofline, "layer_roofline": layer,
+        "kernels_ms": {n: round(v, 4) for n, v in kern_ms.items()},
+        "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, host_inputs(inp))
+    return result
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle as it stands, on the host cores: each step one bounded sample."""
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, device="cpu", seed=0)
+    inp_host = host_inputs(inp)
+    rate0, dt0, _ = oracle_tokens_per_s(w, inp_host, 8)
+    per_step = int(min(w.T, max(8, 8 * 4.0 / max(dt0, 1e-3))))   # ~4 s per step
+    for _ in range(args.warmup):
+        oracle_tokens_per_s(w, inp_host, per_step)
+    total_t, total_n = 0.0, 0
+    for _ in range(args.steps):
+        _, dt, n = oracle_tokens_per_s(w, inp_host, per_step)
+        total_t += dt
+        total_n += n
+    value = total_n / total_t
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_t / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.describe(), "T": w.T, "H": w.H, "I": w.I, "E": w.E, "k": w.k},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} of {w.T} tokens per step (routing + fp64 layer)"},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    rank = int(os.environ.get("RANK", 0))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -49,7 +49,7 @@ class MoeRouteParams(ctypes.Structure):
 
 class MoeWsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("status", "counts", "starts", "offsets", "tile_off1", "tile_off2", "block_hist",
+                ("status", "counts", "starts", "offsets", "tile_off1", "tile_off2", "sched", "block_hist",
                  "perm_src", "perm_inv", "x_perm", "h", "out_perm", "total")] + \
                [("rows", ctypes.c_int64), ("groups", ctypes.c_int32), ("n_chunks", ctypes.c_int32),
                 ("h_ld", ctypes.c_int32), ("reserved", ctypes.c_int32)]

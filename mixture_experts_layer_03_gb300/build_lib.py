@@ -10,6 +10,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -17,7 +18,7 @@ import sys
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
-BUILD_DIR = os.path.join(ROOT, "_build")
+BUILD_DIR = os.path.join(ROOT, "_build", platform.machine())
 LIB_NAME = "libmoe_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 SOURCES = ["api.cu", "route.cu", "permute.cu", "grouped_gemm.cu", "finalize.cu"]

@@ -19,10 +19,16 @@
 // thread's columns c and 128+c (token-major); the SwiGLU epilogue h = silu(gate) * up
 // needs no exchange. FC2 loads w2[e] rows [n0, n0+256) (output channels).
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA
-// issuer, warps 2-5 = epilogue (TMEM lanes 32*(warp%4) .. +31). A 4-stage smem ring
-// (16 KB X + 32 KB W per stage) feeds the MMAs; two 256-column TMEM accumulators let the
-// epilogue of one tile overlap the mainloop of the next.
+// Warp roles (192 threads): warp 0 = TMA producer and tile scheduler, warp 1 = TMEM
+// allocator + MMA issuer, warps 2-5 = epilogue (TMEM lanes 32*(warp%4) .. +31). A 4-stage
+// smem ring (16 KB X + 32 KB W per stage) feeds the MMAs; two 256-column TMEM
+// accumulators let the epilogue of one tile overlap the mainloop of the next.
+//
+// Tiles are claimed dynamically: the producer takes the next index from a global atomic
+// counter and passes it to the MMA and epilogue warps through a small smem ring, so CTAs
+// that run faster (L2 hits, lighter tiles, the nearer die) take more tiles. Claims move
+// through the flattened list in order, so the tiles in flight at any time are neighbours
+// that share weight panels in L2. The last CTA to finish resets the counter.
 //
 // Rows past a group's end inside a tile read the next group's rows (or zero fill past
 // the tensor); they only reach accumulator rows/columns that the epilogue masks.
@@ -46,6 +52,7 @@ constexpr int kAccCols = 256;
 constexpr int kTmemCols = 512;
 constexpr int kThreads = 192;
 constexpr int kMaxGroups = 257;
+constexpr int kSchedDepth = 4;                       // tile indices in flight inside a CTA
 constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * (kXStageBytes + kWStageBytes);
 
 struct GemmArgs {
@@ -59,6 +66,7 @@ struct GemmArgs {
   __nv_bfloat16* out;
   int64_t out_ld;
   int32_t* status;
+  int32_t* sched;           // [0] next tile to claim, [1] CTAs finished (both reset to 0 at exit)
 };
 
 struct Tile {
@@ -122,6 +130,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
+  __shared__ uint64_t sched_full[kSchedDepth], sched_empty[kSchedDepth];
+  __shared__ int s_tile[kSchedDepth];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int32_t s_off[kMaxGroups + 1], s_cnt[kMaxGroups], s_start[kMaxGroups];
@@ -150,6 +160,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
       mbar_init(&tempty_bar[s], 128);
     }
     mbar_init(&drain_bar, 1);
+    for (int s = 0; s < kSchedDepth; ++s) {
+      mbar_init(&sched_full[s], 1);
+      mbar_init(&sched_empty[s], 1 + 4);   // the MMA thread + one arrival per epilogue warp
+    }
     s_abort = 0;
     fence_barrier_init();
   }
@@ -177,7 +191,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int it = 0; ok; ++it) {
+        const int slot = it & (kSchedDepth - 1);
+        if (!mbar_wait(&sched_empty[slot], ((it / kSchedDepth) & 1) ^ 1u, abort)) {
+          flag_timeout(a.status, abort);
+          ok = false;
+          break;
+        }
+        int tile = atomicAdd(a.sched, 1);
+        if (tile >= total) tile = -1;
+        s_tile[slot] = tile;
+        mbar_arrive(&sched_full[slot]);
+        if (tile < 0) break;
         const Tile t = decode_tile(tile, s_off, s_cnt, s_start, a, kFc1);
         const bool shared = t.g >= a.E;
         const CUtensorMap* mw = shared ? &map_ws : &map_w;
@@ -237,7 +262,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
       uint32_t acc_phase = 0;
       bool ok = true;
       const uint32_t sx0 = smem_u32(sX), sw0 = smem_u32(sW);
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int it = 0; ok; ++it) {
+        const int slot = it & (kSchedDepth - 1);
+        if (!mbar_wait(&sched_full[slot], (it / kSchedDepth) & 1, abort)) {
+          flag_timeout(a.status, abort);
+          ok = false;
+          break;
+        }
+        const int tile = *reinterpret_cast<volatile int*>(&s_tile[slot]);
+        mbar_arrive(&sched_empty[slot]);
+        if (tile < 0) break;
         const Tile t = decode_tile(tile, s_off, s_cnt, s_start, a, kFc1);
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort)) {
           flag_timeout(a.status, abort);
@@ -294,7 +328,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
     const int lrow = q * 32 + lane;         // accumulator row (lane) of this thread
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int it = 0;; ++it) {
+      const int slot = it & (kSchedDepth - 1);
+      const bool have = mbar_wait(&sched_full[slot], (it / kSchedDepth) & 1, abort);
+      if (!__all_sync(0xffffffffu, have)) {
+        flag_timeout(a.status, abort);
+        break;
+      }
+      const int tile = *reinterpret_cast<volatile int*>(&s_tile[slot]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sched_empty[slot]);
+      if (tile < 0) break;
       const Tile t = decode_tile(tile, s_off, s_cnt, s_start, a, kFc1);
       const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort);
       // Lanes may leave the poll at different times; tcgen05.ld is warp-collective.
@@ -380,6 +424,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    // Every CTA has claimed its last tile before it gets here; the last one to arrive
+    // resets the counters for the next launch on this workspace.
+    __threadfence();
+    if (atomicAdd(a.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(a.sched, 0);
+      atomicExch(a.sched + 1, 0);
+    }
   }
 }
 
@@ -493,6 +546,7 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
     a.out_ld = p.H;
   }
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
+  a.sched = reinterpret_cast<int32_t*>(ws + L.sched) + (kFc1 ? 0 : 2);
 
   // Upper bound on the device-side tile count: each group has at most
   // floor(m/128) + 1 row tiles.

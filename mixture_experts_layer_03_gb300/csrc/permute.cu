@@ -88,6 +88,7 @@ struct PlanArgs {
   int32_t* perm_src;   // [P]
   int32_t* perm_inv;   // [P]
   int32_t* status;
+  int32_t* sched;      // [4] grouped-GEMM tile counters, zeroed here every forward
 };
 
 __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
       a.tile_off1[G] = tot1;
       a.tile_off2[G] = tot2;
     }
+    if (tid < 4) a.sched[tid] = 0;
   }
   __syncthreads();
 
@@ -240,6 +242,7 @@ moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const vo
   a.perm_src = reinterpret_cast<int32_t*>(ws + L.perm_src);
   a.perm_inv = reinterpret_cast<int32_t*>(ws + L.perm_inv);
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
+  a.sched = reinterpret_cast<int32_t*>(ws + L.sched);
   plan_kernel<<<nb, kPermThreads, 0, s>>>(a);
   const int sms = device_sm_count();
   const int64_t rows = L.rows;

@@ -1,4 +1,5 @@
-// Step 1: routing. One warp per token; lane l holds experts l, l+32, ... (E <= 256).
+// Step 1: routing. One warp selects the experts of one token; the block then computes
+// the weights of all its (token, slot) pairs packed across threads.
 //
 // Methods (RoutingMethodType of the TensorRT-LLM MoE page, section "路由方法枚举"):
 //   Default          softmax over all E, top-k, weights = the selected probabilities
@@ -10,10 +11,20 @@
 //                    sum of the top-2 biased scores, keep topk_group groups, top-k among
 //                    their experts, weights = unbiased scores / (sum + 1e-20) * rsf.
 //
-// Selection keys are fp32 so ids are exact: the logit itself for the softmax and
-// sigmoid methods (both maps are increasing), and fl32(fl32(sigmoid_fp64(l)) + b) for
+// Selection keys are fp32 so ids are exact: the logit itself for the softmax and sigmoid
+// methods (both maps are increasing), and kappa = fl32(fl32(sigmoid_fp64(l)) + b) for
 // DeepSeekV3. Ties go to the lower expert index; slots are listed by descending key.
-// Weights are computed in fp64 and rounded once to fp32.
+//
+// FP64 runs at 1/64 of the FP32 rate on this part, so it is used only where the result
+// depends on it:
+//  * weights: exp/sigmoid of the k selected logits and the divisions, in fp64, for all
+//    (token, slot) pairs of a block packed across threads; the Default normaliser over
+//    all E uses fp32 expf terms (relative error <= 2 ulp each) accumulated in fp64.
+//  * DeepSeekV3 keys: every kappa is first approximated in fp32 (|error| <= D, a bound
+//    with a wide margin); the exact fp64-derived kappa is then computed only for the
+//    experts that can still decide a group's top-2 sum or the final top-k. Every other
+//    expert is provably below the decision threshold, so the ids equal those from exact
+//    keys everywhere.
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
@@ -23,7 +34,7 @@
 namespace moe {
 namespace {
 
-constexpr int kRouteWarps = 8;
+constexpr int kRouteWarps = 4;
 constexpr int kMaxPerLane = 8;    // 256 experts / 32 lanes
 constexpr int kMaxTopK = 8;
 
@@ -40,19 +51,13 @@ __device__ __forceinline__ bool beats(float ka, int ia, float kb, int ib) {
 __device__ __forceinline__ KeyIdx warp_best(KeyIdx v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
-    float ok = __shfl_xor_sync(0xffffffffu, v.key, off);
-    int oi = __shfl_xor_sync(0xffffffffu, v.idx, off);
+    const float ok = __shfl_xor_sync(0xffffffffu, v.key, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, v.idx, off);
     if (beats(ok, oi, v.key, v.idx)) {
       v.key = ok;
       v.idx = oi;
     }
   }
-  return v;
-}
-
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
   return v;
 }
 
@@ -62,165 +67,239 @@ __device__ __forceinline__ float warp_max_f(float v) {
   return v;
 }
 
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
 __device__ __forceinline__ double sigmoid_d(double l) { return 1.0 / (1.0 + exp(-l)); }
+
+__device__ __forceinline__ float exact_kappa(float l, float b) {
+  return __fadd_rn(__double2float_rn(sigmoid_d(static_cast<double>(l))), b);
+}
+
+// k rounds of warp argmax over this lane's keys; returns the winners (uniform in the
+// warp). Keys of absent or excluded experts must be passed as absent via `live`.
+__device__ __forceinline__ void warp_topk(const float (&key)[kMaxPerLane], uint32_t live, int k,
+                                          int lane, int (&sel)[kMaxTopK], float* kth_key) {
+  uint32_t taken = 0;
+  float last = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    sel[j] = 0;
+    if (j < k) {
+      KeyIdx best{-INFINITY, INT32_MAX};
+#pragma unroll
+      for (int i = 0; i < kMaxPerLane; ++i) {
+        const int e = lane + 32 * i;
+        if (((live & ~taken) >> i) & 1u && beats(key[i], e, best.key, best.idx)) {
+          best.key = key[i];
+          best.idx = e;
+        }
+      }
+      best = warp_best(best);
+      if (best.idx == INT32_MAX) best.idx = 0;   // unreachable: callers pass >= k live keys
+      if ((best.idx & 31) == lane) taken |= 1u << (best.idx >> 5);
+      sel[j] = best.idx;
+      last = best.key;
+    }
+  }
+  if (kth_key) *kth_key = last;
+}
 
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __restrict__ bias,
              int method, int k, int n_group, int topk_group, float rsf,
              int32_t* __restrict__ ids, float* __restrict__ scales) {
   __shared__ float s_key[kRouteWarps][256];
+  __shared__ uint8_t s_exact[kRouteWarps][256];
+  __shared__ float s_sel_l[kRouteWarps][kMaxTopK];
+  __shared__ double s_e[kRouteWarps][kMaxTopK];
+  __shared__ double s_z[kRouteWarps];
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp;
-  if (t >= T) return;   // warp-uniform
-  const float* row = logits + t * E;
+  const bool valid = t < T;   // warp-uniform; invalid warps still reach the block barriers
 
-  // Load: l = logit (non-finite -> -inf), key = selection key.
-  float l[kMaxPerLane], key[kMaxPerLane];
-  bool present[kMaxPerLane];
-#pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
-    const int e = lane + 32 * i;
-    present[i] = e < E;
-    float v = present[i] ? row[e] : -INFINITY;
-    if (!isfinite(v)) v = -INFINITY;
-    l[i] = v;
-    if (method == MOE_ROUTE_DEEPSEEKV3 && present[i]) {
-      const float s32 = __double2float_rn(sigmoid_d(static_cast<double>(v)));
-      key[i] = __fadd_rn(s32, bias ? bias[e] : 0.0f);
-    } else {
-      key[i] = v;
-    }
-  }
-
-  if (method == MOE_ROUTE_DEEPSEEKV3) {
-    // Group scores: lane g < n_group sums the top-2 keys of its group.
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i)
-      if (present[i]) s_key[warp][lane + 32 * i] = key[i];
-    __syncwarp();
-    const int epg = E / n_group;
-    float gscore = -INFINITY;
-    int gidx = INT32_MAX;
-    if (lane < n_group) {
-      float a = -INFINITY, b = -INFINITY;   // a >= b: the two largest
-      for (int j = 0; j < epg; ++j) {
-        const float v = s_key[warp][lane * epg + j];
-        if (v > a) {
-          b = a;
-          a = v;
-        } else if (v > b) {
-          b = v;
-        }
-      }
-      gscore = __fadd_rn(a, b);
-      gidx = lane;
-    }
-    // Keep topk_group groups: repeated warp argmax.
-    uint32_t chosen = 0;
-    bool taken = false;
-    for (int r = 0; r < topk_group; ++r) {
-      KeyIdx v = taken ? KeyIdx{-INFINITY, INT32_MAX} : KeyIdx{gscore, gidx};
-      v = warp_best(v);
-      if (v.idx == lane) taken = true;
-      chosen |= 1u << v.idx;
-    }
-    // Experts outside the chosen groups cannot be selected.
+  if (valid) {
+    const float* row = logits + t * E;
+    float l[kMaxPerLane], key[kMaxPerLane];
+    uint32_t present = 0;
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
       const int e = lane + 32 * i;
-      if (present[i] && !((chosen >> (e / epg)) & 1u)) key[i] = -INFINITY;
+      float v = -INFINITY;
+      if (e < E) {
+        present |= 1u << i;
+        v = row[e];
+        if (!isfinite(v)) v = -INFINITY;
+      }
+      l[i] = v;
+      key[i] = v;
     }
-  }
 
-  // Top-k by repeated warp argmax; every lane ends with the same sel_* arrays.
-  int sel_idx[kMaxTopK];
-  float sel_l[kMaxTopK];
-  uint32_t taken_mask = 0;
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    sel_idx[j] = 0;
-    sel_l[j] = 0.f;
-    if (j < k) {
-      KeyIdx best{-INFINITY, INT32_MAX};
+    if (method == MOE_ROUTE_DEEPSEEKV3) {
+      // fp32 approximation of every kappa, and a bound D on |kappa_exact - kappa_approx|:
+      // the fp32 sigmoid is within 4e-7 of the true value and both roundings add at most
+      // one ulp of the key, so 1e-6 + 2.5e-7 * |kappa| holds with room to spare.
+      float amax = 0.f;
 #pragma unroll
       for (int i = 0; i < kMaxPerLane; ++i) {
         const int e = lane + 32 * i;
-        if (present[i] && !((taken_mask >> i) & 1u) && beats(key[i], e, best.key, best.idx)) {
-          best.key = key[i];
-          best.idx = e;
+        if ((present >> i) & 1u) {
+          const float b = bias ? bias[e] : 0.0f;
+          const bool fin = l[i] != -INFINITY;
+          const float sa = fin ? 1.0f / (1.0f + expf(-l[i])) : 0.0f;
+          key[i] = __fadd_rn(sa, b);
+          s_key[warp][e] = key[i];
+          s_exact[warp][e] = fin ? 0 : 1;   // sigmoid(-inf) = 0 exactly
+          amax = fmaxf(amax, fabsf(key[i]));
         }
       }
-      best = warp_best(best);
-      const int owner = best.idx & 31;
-      const int slot = best.idx >> 5;
-      float lv = 0.f;
-#pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i)
-        if (i == slot) lv = l[i];
-      lv = __shfl_sync(0xffffffffu, lv, owner);
-      if (lane == owner) taken_mask |= 1u << slot;
-      sel_idx[j] = best.idx;
-      sel_l[j] = lv;
-    }
-  }
+      const float D = 1e-6f + 2.5e-7f * warp_max_f(amax);
+      __syncwarp();
 
-  // Weights in fp64.
-  double w[kMaxTopK];
-  if (method == MOE_ROUTE_DEFAULT || method == MOE_ROUTE_RENORMALIZE_NAIVE) {
-    float m = -INFINITY;
+      // Group scores: lane g sums the exact top-2 keys of its group. Only experts whose
+      // approximate key is within 2D of the approximate second-largest can be in the
+      // exact top-2; their keys are made exact first.
+      const int epg = E / n_group;
+      float gscore = -INFINITY;
+      int gidx = INT32_MAX;
+      if (lane < n_group) {
+        const int e0 = lane * epg;
+        float a1 = -INFINITY, a2 = -INFINITY;
+        for (int j = 0; j < epg; ++j) {
+          const float v = s_key[warp][e0 + j];
+          if (v > a1) { a2 = a1; a1 = v; } else if (v > a2) { a2 = v; }
+        }
+        const float thr = a2 - 2.0f * D;
+        float x1 = -INFINITY, x2 = -INFINITY;
+        for (int j = 0; j < epg; ++j) {
+          const int e = e0 + j;
+          float v = s_key[warp][e];
+          if (v >= thr) {
+            if (!s_exact[warp][e]) {
+              v = exact_kappa(row[e], bias ? bias[e] : 0.0f);
+              s_key[warp][e] = v;
+              s_exact[warp][e] = 1;
+            }
+            if (v > x1) { x2 = x1; x1 = v; } else if (v > x2) { x2 = v; }
+          }
+        }
+        gscore = __fadd_rn(x1, x2);
+        gidx = lane;
+      }
+      // Keep topk_group groups by repeated warp argmax (ties: lower group index).
+      uint32_t chosen = 0;
+      bool gtaken = false;
+      for (int r = 0; r < topk_group; ++r) {
+        KeyIdx v = gtaken ? KeyIdx{-INFINITY, INT32_MAX} : KeyIdx{gscore, gidx};
+        v = warp_best(v);
+        if (v.idx == lane) gtaken = true;
+        chosen |= 1u << v.idx;
+      }
+      __syncwarp();
+
+      // Final top-k inside the chosen groups. Bounds per expert (exact: lb = ub = kappa);
+      // the k-th largest lower bound is a threshold no non-candidate can reach.
+      float lb[kMaxPerLane];
+      uint32_t live = 0;
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) m = fmaxf(m, l[i]);
-    m = warp_max_f(m);
-    double z = 0.0;
+      for (int i = 0; i < kMaxPerLane; ++i) {
+        const int e = lane + 32 * i;
+        lb[i] = -INFINITY;
+        if (((present >> i) & 1u) && ((chosen >> (e / epg)) & 1u)) {
+          live |= 1u << i;
+          key[i] = s_key[warp][e];
+          lb[i] = s_exact[warp][e] ? key[i] : key[i] - D;
+        }
+      }
+      int tmp[kMaxTopK];
+      float kth_lb;
+      warp_topk(lb, live, k, lane, tmp, &kth_lb);
+      uint32_t cand = 0;
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i)
-      if (present[i]) z += exp(static_cast<double>(l[i]) - static_cast<double>(m));
-    z = warp_sum_d(z);
-    double psum = 0.0;
+      for (int i = 0; i < kMaxPerLane; ++i) {
+        const int e = lane + 32 * i;
+        if ((live >> i) & 1u) {
+          const bool ex = s_exact[warp][e];
+          const float ub = ex ? key[i] : key[i] + D;
+          if (ub >= kth_lb) {
+            cand |= 1u << i;
+            if (!ex) key[i] = exact_kappa(row[e], bias ? bias[e] : 0.0f);
+          }
+        }
+      }
+      int sel[kMaxTopK];
+      warp_topk(key, cand, k, lane, sel, nullptr);
+      // Selected logits for the weights.
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      w[j] = (j < k) ? exp(static_cast<double>(sel_l[j]) - static_cast<double>(m)) / z : 0.0;
-      psum += w[j];
-    }
-    if (method == MOE_ROUTE_RENORMALIZE_NAIVE) {
-#pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) w[j] /= psum;
-    }
-  } else if (method == MOE_ROUTE_RENORMALIZE) {
-    const double m = static_cast<double>(sel_l[0]);
-    double z = 0.0;
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      w[j] = (j < k) ? exp(static_cast<double>(sel_l[j]) - m) : 0.0;
-      z += w[j];
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) w[j] /= z;
-  } else {   // SigmoidRenorm, DeepSeekV3: unbiased sigmoid of the selected logits
-    double z = 0.0;
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      w[j] = (j < k) ? sigmoid_d(static_cast<double>(sel_l[j])) : 0.0;
-      z += w[j];
-    }
-    if (method == MOE_ROUTE_DEEPSEEKV3) {
-      const double denom = z + 1e-20;
-#pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) w[j] = w[j] / denom * static_cast<double>(rsf);
+      for (int j = 0; j < kMaxTopK; ++j) {
+        if (j < k && lane == j) {
+          ids[t * k + j] = sel[j];
+          const float v = row[sel[j]];
+          s_sel_l[warp][j] = isfinite(v) ? v : -INFINITY;
+        }
+      }
     } else {
+      int sel[kMaxTopK];
+      warp_topk(key, present, k, lane, sel, nullptr);
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) w[j] /= z;
+      for (int j = 0; j < kMaxTopK; ++j) {
+        if (j < k && lane == j) {
+          ids[t * k + j] = sel[j];
+          const float v = row[sel[j]];
+          s_sel_l[warp][j] = isfinite(v) ? v : -INFINITY;
+        }
+      }
+      if (method == MOE_ROUTE_DEFAULT) {
+        // Normaliser over all E: fp32 exp terms, fp64 accumulation.
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i) m = fmaxf(m, l[i]);
+        m = warp_max_f(m);
+        double z = 0.0;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i)
+          if ((present >> i) & 1u) z += static_cast<double>(expf(l[i] - m));
+        z = warp_sum_d(z);
+        if (lane == 0) s_z[warp] = z;
+      }
     }
   }
+  __syncthreads();
 
-  // Lane j < k writes slot j.
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    if (j < k && lane == j) {
-      ids[t * k + j] = sel_idx[j];
-      scales[t * k + j] = __double2float_rn(w[j]);
-    }
+  // Weights of the block's (token, slot) pairs, packed across threads.
+  const int npairs = kRouteWarps * k;
+  for (int pidx = threadIdx.x; pidx < npairs; pidx += blockDim.x) {
+    const int w = pidx / k, j = pidx - w * k;
+    const int64_t tt = static_cast<int64_t>(blockIdx.x) * kRouteWarps + w;
+    if (tt >= T) continue;
+    const double lv = static_cast<double>(s_sel_l[w][j]);
+    double e;
+    if (method == MOE_ROUTE_SIGMOID_RENORM || method == MOE_ROUTE_DEEPSEEKV3)
+      e = sigmoid_d(lv);
+    else
+      e = exp(lv - static_cast<double>(s_sel_l[w][0]));   // slot 0 holds the largest logit
+    s_e[w][j] = e;
+  }
+  __syncthreads();
+  for (int pidx = threadIdx.x; pidx < npairs; pidx += blockDim.x) {
+    const int w = pidx / k, j = pidx - w * k;
+    const int64_t tt = static_cast<int64_t>(blockIdx.x) * kRouteWarps + w;
+    if (tt >= T) continue;
+    double s = 0.0;
+    for (int q = 0; q < k; ++q) s += s_e[w][q];
+    double wgt;
+    if (method == MOE_ROUTE_DEFAULT)
+      wgt = s_e[w][j] / s_z[w];
+    else if (method == MOE_ROUTE_DEEPSEEKV3)
+      wgt = s_e[w][j] / (s + 1e-20) * static_cast<double>(rsf);
+    else
+      wgt = s_e[w][j] / s;
+    scales[tt * k + j] = __double2float_rn(wgt);
   }
 }
 

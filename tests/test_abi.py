@@ -18,8 +18,8 @@ def moe():
     if not os.path.exists(lib_path):
         if not (shutil.which("nvcc") or os.path.exists("/usr/local/cuda/bin/nvcc")):
             pytest.skip("library not built and nvcc unavailable")
-        from mixture_experts_layer_03_gb300 import build_lib
-        build_lib.build()
+        import __graft_entry__
+        __graft_entry__.build()
     import mixture_experts_layer_03_gb300 as m
     return m
 
@@ -75,7 +75,7 @@ def test_workspace_layout(moe):
     L = moe.moe_workspace_layout(p)
     P, R = 512 * 8, 512 * 8 + 512
     assert L["rows"] == R and L["groups"] == 257 and L["h_ld"] == 2048 and L["n_chunks"] == 1
-    names = ["status", "counts", "starts", "offsets", "tile_off1", "tile_off2", "block_hist",
+    names = ["status", "counts", "starts", "offsets", "tile_off1", "tile_off2", "sched", "block_hist",
              "perm_src", "perm_inv", "x_perm", "h", "out_perm", "total"]
     offs = [L[n] for n in names]
     assert offs == sorted(offs) and all(o % 1024 == 0 for o in offs)
