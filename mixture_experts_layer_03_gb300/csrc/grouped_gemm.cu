@@ -44,10 +44,12 @@
 namespace moe {
 namespace {
 
-constexpr int kBK = 64;                              // K per stage: one 128-byte row
+constexpr int kBK = 64;                              // K elements per stage
+constexpr int kRowBytes = kBK * 2;                   // one K row of a tile = the swizzle width
 constexpr int kStages = 4;
-constexpr int kXStageBytes = 128 * kBK * 2;          // 16 KB
-constexpr int kWStageBytes = 256 * kBK * 2;          // 32 KB
+constexpr int kXStageBytes = 128 * kRowBytes;        // 128 rows of X
+constexpr int kWHalfBytes = 128 * kRowBytes;         // 128 rows of W
+constexpr int kWStageBytes = 2 * kWHalfBytes;
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 512;
 constexpr int kThreads = 192;
@@ -143,7 +145,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint8_t* sX = smem;                                   // kStages x 16 KB
-  uint8_t* sW = smem + kStages * kXStageBytes;          // kStages x 32 KB
+  uint8_t* sW = smem + kStages * kXStageBytes;          // kStages x 256 W rows
 
   for (int i = threadIdx.x; i <= a.G; i += blockDim.x) s_off[i] = a.tile_off[i];
   for (int i = threadIdx.x; i < a.G; i += blockDim.x) {
@@ -210,7 +212,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
         const int wr0 = t.n0;
         const int wr1 = kFc1 ? (t.N + t.n0) : (t.n0 + 128);
         const uint32_t bytes =
-            kWStageBytes + (t.token_major ? kXStageBytes : static_cast<uint32_t>(t.ntok) * 128u);
+            kWStageBytes + (t.token_major ? kXStageBytes : static_cast<uint32_t>(t.ntok) * kRowBytes);
         const int nkb = t.K / kBK;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort)) {
@@ -226,10 +228,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
             tma_load_2d(xs, &map_x128, &full_bar[stage], kc, t.row0);
           } else {
             for (int r = 0; r < t.ntok; r += 16)
-              tma_load_2d(xs + r * 128, &map_x16, &full_bar[stage], kc, t.row0 + r);
+              tma_load_2d(xs + r * kRowBytes, &map_x16, &full_bar[stage], kc, t.row0 + r);
           }
           tma_load_3d(ws, mw, &full_bar[stage], kc, wr0, ecoord);
-          tma_load_3d(ws + 128 * 128, mw, &full_bar[stage], kc, wr1, ecoord);
+          tma_load_3d(ws + kWHalfBytes, mw, &full_bar[stage], kc, wr1, ecoord);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -294,12 +296,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t accum = (kb | kk) != 0;
-            const uint64_t dx = sdesc_k_sw128(xa + kk * 32);
+            const uint64_t dx = sdesc_k_major(xa + kk * 32, kRowBytes);
             if (t.token_major) {
-              umma_bf16(d, dx, sdesc_k_sw128(wa + kk * 32), idesc, accum);
+              umma_bf16(d, dx, sdesc_k_major(wa + kk * 32, kRowBytes), idesc, accum);
             } else {
-              umma_bf16(d, sdesc_k_sw128(wa + kk * 32), dx, idesc, accum);
-              umma_bf16(d + 128, sdesc_k_sw128(wa + 128 * 128 + kk * 32), dx, idesc, accum);
+              umma_bf16(d, sdesc_k_major(wa + kk * 32, kRowBytes), dx, idesc, accum);
+              umma_bf16(d + 128, sdesc_k_major(wa + kWHalfBytes + kk * 32, kRowBytes), dx, idesc,
+                        accum);
             }
           }
           umma_commit(&empty_bar[stage]);
@@ -438,6 +441,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
 
 // ---------------------------------------------------------------- host side
 
+constexpr CUtensorMapSwizzle kSwizzle =
+    kRowBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -463,10 +469,10 @@ bool encode_map2(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {kBK, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, kSwizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -478,10 +484,10 @@ bool encode_map3(CUtensorMap* m, const void* base, uint64_t planes, uint64_t row
   if (!enc) return false;
   cuuint64_t dims[3] = {cols, rows, planes};
   cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
-  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t box[3] = {kBK, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, kSwizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

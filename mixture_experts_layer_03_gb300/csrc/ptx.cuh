@@ -158,6 +158,22 @@ __device__ __forceinline__ void tma_load_3d_multicast(void* dst, const CUtensorM
       : "memory");
 }
 
+// Bulk prefetch of a 2-D / 3-D tile into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                int32_t c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 // Whole-warp TMEM allocation; the TMEM address lands in *slot (shared memory).
@@ -221,17 +237,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Shared-memory matrix descriptor for a K-major tile written by TMA with the
-// 128-byte swizzle: rows of 128 bytes, 8-row swizzle atoms of 1024 bytes
-// (stride byte offset), leading byte offset unused (1), descriptor version 1
-// (bits 46-48 = 0b001), swizzle mode 2 = 128B (bits 61-63).
-__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+// Shared-memory matrix descriptor for a K-major tile written by TMA with a swizzle as
+// wide as one K row (128 or 64 bytes): 8-row swizzle atoms, so the stride byte offset
+// is 8 rows; the leading byte offset is unused for this layout (1); descriptor version 1
+// (bits 46-48 = 0b001); swizzle mode at bits 61-63: 2 = 128-byte, 4 = 64-byte.
+// Advancing the start address by 32 bytes steps K by 16 bf16 elements inside the atom.
+__device__ __forceinline__ uint64_t sdesc_k_major(uint32_t saddr, uint32_t row_bytes) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>(1) << 16;
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>((8u * row_bytes) >> 4) << 32;
   d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
+  d |= static_cast<uint64_t>(row_bytes == 128 ? 2 : 4) << 61;
   return d;
 }
 
