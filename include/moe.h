@@ -181,6 +181,30 @@ moe_status moe_forward(const moe_problem* p, const void* x, const int32_t* ids, 
                        const void* w13, const void* w2, const void* w13_s, const void* w2_s,
                        void* y, void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * moe_forward_static -- moe_forward without a caller workspace. The pages have no
+ * counterpart; this entry point exists for callers that cannot allocate device memory:
+ * plugins hosted by an inference engine that owns every device allocation, and
+ * latency-critical loops that must not call cudaMalloc (it can synchronise the whole
+ * device). The scratch the forward needs lives in a fixed array inside this library,
+ * MOE_STATIC_SCRATCH_BYTES bytes on every GPU that loads it, held until the process
+ * exits. Arguments are those of moe_forward minus the workspace.
+ *  - Problems whose workspace (moe_workspace_bytes) exceeds MOE_STATIC_SCRATCH_BYTES are
+ *    rejected with MOE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *  - The first call on a device looks up the array's device address (once per device,
+ *    with that device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array and it keeps the previous call's
+ *    contents (the call clears what must start at zero itself). Calls whose work
+ *    overlaps on the GPU race: order them on one stream.
+ *  - Device-detected errors (ids outside [0, E)) skip rows as in moe_forward; their
+ *    status bits stay in the library's array and are not reported.
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ */
+#define MOE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+moe_status moe_forward_static(const moe_problem* p, const void* x, const int32_t* ids,
+                              const float* scales, const void* w13, const void* w2,
+                              const void* w13_s, const void* w2_s, void* y, void* stream);
+
 /* Step entry points (the kernels moe_forward runs, one at a time). Each takes the
  * same workspace; later steps read what earlier ones wrote into it. */
 

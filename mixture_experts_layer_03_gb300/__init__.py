@@ -67,6 +67,8 @@ _SIGS = {
     "moe_workspace_layout": (ctypes.c_int, [ctypes.POINTER(MoeProblem), ctypes.POINTER(MoeWsLayout)]),
     "moe_forward": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    ctypes.c_size_t, _P]),
+    "moe_forward_static": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, _P, _P, _P, _P,
+                                          _P, _P]),
     "moe_permute": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_fc1": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_fc2": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
@@ -216,6 +218,33 @@ def moe_forward(x, ids, scales, w13, w2, w13_s=None, w2_s=None, y=None,
     _check(_lib.moe_forward(ctypes.byref(p), _ptr(x), _ptr(ids), _ptr(scales), _ptr(w13), _ptr(w2),
                             _ptr(w13_s), _ptr(w2_s), _ptr(y), workspace.ptr, workspace.nbytes,
                             _stream(stream)), "moe_forward")
+    return y
+
+
+MOE_STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def moe_forward_static(x, ids, scales, w13, w2, w13_s=None, w2_s=None, y=None, stream=None):
+    """moe_forward with the library's built-in scratch instead of a caller workspace.
+
+    For callers that cannot allocate device memory (a plugin whose host engine owns all
+    device allocations, or a loop that must not call cudaMalloc). Problems whose workspace
+    exceeds MOE_STATIC_SCRATCH_BYTES are rejected. All calls on a GPU share one scratch
+    array, so calls that overlap on the GPU race; the first call on a device sets the
+    array up and should come before any stream capture. ``y`` is allocated here (by
+    torch) only when the caller does not pass it.
+    """
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(ids, "ids", torch.int32)
+    _cuda(scales, "scales", torch.float32)
+    _cuda(w13, "w13", torch.bfloat16)
+    _cuda(w2, "w2", torch.bfloat16)
+    p = _problem_for(x, ids, w13, w2, w13_s)
+    if y is None:
+        y = torch.empty_like(x)
+    _check(_lib.moe_forward_static(ctypes.byref(p), _ptr(x), _ptr(ids), _ptr(scales), _ptr(w13),
+                                   _ptr(w2), _ptr(w13_s), _ptr(w2_s), _ptr(y), _stream(stream)),
+           "moe_forward_static")
     return y
 
 

@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -249,6 +250,73 @@ moe_status moe_forward(const moe_problem* p, const void* x, const int32_t* ids, 
     return set_error(MOE_ERR_INVALID_ARG, "shared expert weights NULL or not 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
+  if ((st = launch_permute(*p, L, x, ids, ws, s)) != MOE_OK) return st;
+  if ((st = launch_fc1(*p, L, w13, w13_s, ws, s)) != MOE_OK) return st;
+  if ((st = launch_fc2(*p, L, w2, w2_s, ws, s)) != MOE_OK) return st;
+  return launch_finalize(*p, L, scales, y, ws, s);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Scratch of moe_forward_static: one fixed array per GPU, in this library's device
+// image. The extra 1024 bytes let the workspace start on a 1024-byte boundary.
+__device__ __align__(256) unsigned char g_static_scratch[MOE_STATIC_SCRATCH_BYTES + 1024];
+
+std::mutex g_static_mu;
+void* g_static_addr[64] = {nullptr};
+
+// Device address of g_static_scratch on the current device, looked up once per device
+// with that device current (the symbol's name is only a host-side stand-in).
+moe_status static_scratch_base(char** base) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64)
+    return set_error(MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_static_scratch);
+    if (e != cudaSuccess || !addr)
+      return set_error(MOE_ERR_CUDA, "cudaGetSymbolAddress(static scratch): %s", cudaGetErrorString(e));
+    g_static_addr[dev] = addr;
+  }
+  const uintptr_t a = reinterpret_cast<uintptr_t>(g_static_addr[dev]);
+  *base = reinterpret_cast<char*>((a + 1023u) & ~static_cast<uintptr_t>(1023u));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_forward_static(const moe_problem* p, const void* x, const int32_t* ids,
+                              const float* scales, const void* w13, const void* w2,
+                              const void* w13_s, const void* w2_s, void* y, void* stream) {
+  if (!p) return set_error(MOE_ERR_INVALID_ARG, "problem is NULL");
+  const int32_t reason = problem_reason(*p);
+  if (reason != MOE_REASON_OK)
+    return set_error(MOE_ERR_UNSUPPORTED, "problem outside the supported envelope (reason %d)", reason);
+  moe_ws_layout L;
+  compute_layout(*p, &L);
+  if (p->T == 0) return MOE_OK;
+  if (L.total > MOE_STATIC_SCRATCH_BYTES)
+    return set_error(MOE_ERR_WORKSPACE_TOO_SMALL,
+                     "problem needs %zu bytes of scratch; the static scratch holds %zu", L.total,
+                     static_cast<size_t>(MOE_STATIC_SCRATCH_BYTES));
+  if (!x || !ids || !scales || !w13 || !w2 || !y)
+    return set_error(MOE_ERR_INVALID_ARG, "NULL tensor argument");
+  if (!aligned16(x) || !aligned16(ids) || !aligned16(scales) || !aligned16(w13) || !aligned16(w2) ||
+      !aligned16(y))
+    return set_error(MOE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (!shared_args_ok(p, w13_s, w2_s))
+    return set_error(MOE_ERR_INVALID_ARG, "shared expert weights NULL or not 16-byte aligned");
+  char* ws = nullptr;
+  moe_status st = static_scratch_base(&ws);
+  if (st != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The permute step clears the status word and the GEMM tile counters in the scratch.
   if ((st = launch_permute(*p, L, x, ids, ws, s)) != MOE_OK) return st;
   if ((st = launch_fc1(*p, L, w13, w13_s, ws, s)) != MOE_OK) return st;
   if ((st = launch_fc2(*p, L, w2, w2_s, ws, s)) != MOE_OK) return st;
