@@ -19,7 +19,6 @@ import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
 if "OPENBLAS_NUM_THREADS" not in os.environ:   # the CPU oracle uses every host core
@@ -153,6 +152,22 @@ def cpu_baseline(w: Workload, inp_host: dict, target_s: float = 10.0):
             "sample": f"{n} of {w.T} tokens of {w.name} (routing + fp64 layer), {dt:.1f} s"}
 
 
+# --------------------------------------------------------------------------- ranks
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, steps: int, max_total_ms: float, world: int) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (max_total_ms / 1e3)
+
+
 # --------------------------------------------------------------------------- our arm
 
 def traffic_record(kernel_file: str, workload: str):
@@ -235,13 +250,9 @@ def run_ours(args, rank, world):
         barrier()
     clocks = clk.summary()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * w.T * args.steps / (total_ms / 1e3)
+    value = job_tokens_per_s(w.T, args.steps, total_ms, world)
 
     # ---- per-kernel durations: the same kernels through the step entry points, queued
     # behind a sleep kernel so each event pair brackets device time only.
@@ -288,12 +299,8 @@ def run_ours(args, rank, world):
         y_h.copy_(y, non_blocking=True)
         ee[i][1].record(stream)
     barrier()
-    e2e_total = sum(a.elapsed_time(b) for a, b in ee)
-    if world > 1:
-        t = torch.tensor([e2e_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e = {"value": round(world * w.T * args.steps / (e2e_total / 1e3), 1), "unit": UNIT,
+    e2e_total = reduce_max(sum(a.elapsed_time(b) for a, b in ee), world, dev)
+    e2e = {"value": round(job_tokens_per_s(w.T, args.steps, e2e_total, world), 1), "unit": UNIT,
            "h2d_bytes_per_step": x.numel() * x.element_size() + logits.numel() * 4,
            "d2h_bytes_per_step": y.numel() * y.element_size(),
            "how": "eager moe_route + moe_forward calls, pinned host x/logits in and y out each step"}
