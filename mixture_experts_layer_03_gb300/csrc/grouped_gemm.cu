@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "launch.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -147,11 +148,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
   uint8_t* sX = smem;                                   // kStages x 16 KB
   uint8_t* sW = smem + kStages * kXStageBytes;          // kStages x 256 W rows
 
-  for (int i = threadIdx.x; i <= a.G; i += blockDim.x) s_off[i] = a.tile_off[i];
-  for (int i = threadIdx.x; i < a.G; i += blockDim.x) {
-    s_cnt[i] = a.counts[i];
-    s_start[i] = a.starts[i];
-  }
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -178,6 +175,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
   if (warp == 1) {
     tmem_alloc(&s_tmem_base, kTmemCols);
     tmem_relinquish();
+  }
+  // Everything above overlaps the previous kernel; the work lists are its output.
+  pdl_wait();
+  for (int i = threadIdx.x; i <= a.G; i += blockDim.x) s_off[i] = a.tile_off[i];
+  for (int i = threadIdx.x; i < a.G; i += blockDim.x) {
+    s_cnt[i] = a.counts[i];
+    s_start[i] = a.starts[i];
   }
   tc_fence_before();
   __syncthreads();
@@ -562,8 +566,8 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
   int64_t grid = device_sm_count();
   if (grid > bound) grid = bound;
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<kFc1><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(mx128, mx16, mw, mws, a);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(grouped_gemm_kernel<kFc1>, dim3(static_cast<unsigned>(grid)),
+                               dim3(kThreads), kSmemBytes, s, mx128, mx16, mw, mws, a);
   if (err != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "grouped_gemm launch: %s", cudaGetErrorString(err));
   return MOE_OK;

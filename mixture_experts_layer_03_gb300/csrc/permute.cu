@@ -4,6 +4,7 @@
 //
 // Deterministic, no atomics in the ordering:
 //   hist_kernel    per chunk of kPermChunk (token, slot) pairs: histogram over experts
+//                  (skipped when there is a single chunk: the plan kernel counts it)
 //   plan_kernel    every chunk: column sums + exclusive scan of the histograms give each
 //                  (chunk, expert) its base row; inside the chunk, ranks come from
 //                  warp match_any and a running per-expert count, so rows of an expert
@@ -16,6 +17,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "launch.cuh"
 
 namespace moe {
 namespace {
@@ -23,9 +25,14 @@ namespace {
 constexpr int kPermWarps = kPermThreads / 32;
 
 __global__ void __launch_bounds__(kPermThreads)
-hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int32_t* __restrict__ block_hist) {
+hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int32_t* __restrict__ block_hist,
+            int32_t* __restrict__ status) {
   __shared__ int32_t h[256];
+  pdl_trigger();
   for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+  pdl_wait();
+  // This forward's status bits start from zero (the plan and GEMM kernels run after).
+  if (blockIdx.x == 0 && threadIdx.x < 4) status[threadIdx.x] = 0;
   __syncthreads();
   const int64_t f0 = static_cast<int64_t>(blockIdx.x) * kPermChunk;
   const int64_t f1 = (P < f0 + kPermChunk ? P : f0 + kPermChunk);
@@ -91,6 +98,9 @@ struct PlanArgs {
   int32_t* sched;      // [4] grouped-GEMM tile counters, zeroed here every forward
 };
 
+// kSingleChunk: the whole problem is one chunk (one block); the block counts its own
+// histogram and clears the status word, and no hist_kernel runs before it.
+template <bool kSingleChunk>
 __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
   __shared__ int32_t s_run[256];                // next free row per expert in this chunk
   __shared__ int32_t s_wcnt[kPermWarps][256];   // rows per (warp, expert) in a sub-chunk
@@ -98,10 +108,23 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
   const int tid = threadIdx.x;
   const int b = blockIdx.x;
   const int E = a.E;
+  pdl_trigger();
+  pdl_wait();
 
   // Column sums and this chunk's prefix over earlier chunks.
   int tot = 0, before = 0;
-  if (tid < E) {
+  if (kSingleChunk) {
+    for (int e = tid; e < 256; e += blockDim.x) s_run[e] = 0;
+    if (tid < 4) a.status[tid] = 0;
+    __syncthreads();
+    for (int64_t f = tid; f < a.P; f += blockDim.x) {
+      const int e = a.ids[f];
+      if (e >= 0 && e < E) atomicAdd(&s_run[e], 1);
+    }
+    __syncthreads();
+    if (tid < E) tot = s_run[tid];
+    __syncthreads();
+  } else if (tid < E) {
     for (int c = 0; c < a.nb; ++c) {
       const int v = a.block_hist[c * E + tid];
       if (c < b) before += v;
@@ -196,6 +219,8 @@ gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ p
               int H, __nv_bfloat16* __restrict__ x_perm) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  pdl_trigger();
+  pdl_wait();
   const int64_t p_valid = offsets[E];
   const int nvec = H / 8;
   for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -218,10 +243,7 @@ gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ p
 moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const void* x,
                           const int32_t* ids, char* ws, cudaStream_t s) {
   const int64_t P = p.T * p.k;
-  cudaError_t err = cudaMemsetAsync(ws + L.status, 0, 16, s);
-  if (err != cudaSuccess) return set_error(MOE_ERR_CUDA, "status clear: %s", cudaGetErrorString(err));
   const int nb = L.n_chunks;
-  hist_kernel<<<nb, kPermThreads, 0, s>>>(ids, P, p.E, reinterpret_cast<int32_t*>(ws + L.block_hist));
   PlanArgs a;
   a.ids = ids;
   a.P = P;
@@ -243,15 +265,24 @@ moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const vo
   a.perm_inv = reinterpret_cast<int32_t*>(ws + L.perm_inv);
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
   a.sched = reinterpret_cast<int32_t*>(ws + L.sched);
-  plan_kernel<<<nb, kPermThreads, 0, s>>>(a);
-  const int sms = device_sm_count();
-  const int64_t rows = L.rows;
-  int64_t blocks = (rows + 7) / 8;
-  if (blocks > static_cast<int64_t>(sms) * 16) blocks = static_cast<int64_t>(sms) * 16;
-  gather_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(x), a.perm_src, a.offsets, P, p.E, p.k, rows, p.H,
-      reinterpret_cast<__nv_bfloat16*>(ws + L.x_perm));
-  err = cudaGetLastError();
+  cudaError_t err;
+  if (nb == 1) {
+    err = launch_pdl(plan_kernel<true>, dim3(1), dim3(kPermThreads), 0, s, a);
+  } else {
+    err = launch_pdl(hist_kernel, dim3(nb), dim3(kPermThreads), 0, s, ids, P, p.E,
+                     reinterpret_cast<int32_t*>(ws + L.block_hist), a.status);
+    if (err == cudaSuccess) err = launch_pdl(plan_kernel<false>, dim3(nb), dim3(kPermThreads), 0, s, a);
+  }
+  if (err == cudaSuccess) {
+    const int sms = device_sm_count();
+    const int64_t rows = L.rows;
+    int64_t blocks = (rows + 7) / 8;
+    if (blocks > static_cast<int64_t>(sms) * 16) blocks = static_cast<int64_t>(sms) * 16;
+    err = launch_pdl(gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                     static_cast<const __nv_bfloat16*>(x), static_cast<const int32_t*>(a.perm_src),
+                     static_cast<const int32_t*>(a.offsets), P, p.E, p.k, rows, p.H,
+                     reinterpret_cast<__nv_bfloat16*>(ws + L.x_perm));
+  }
   if (err != cudaSuccess) return set_error(MOE_ERR_CUDA, "permute launch: %s", cudaGetErrorString(err));
   return MOE_OK;
 }

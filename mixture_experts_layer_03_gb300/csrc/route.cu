@@ -30,12 +30,12 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "launch.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kRouteWarps = 4;
-constexpr int kMaxPerLane = 8;    // 256 experts / 32 lanes
 constexpr int kMaxTopK = 8;
 
 struct KeyIdx {
@@ -81,7 +81,8 @@ __device__ __forceinline__ float exact_kappa(float l, float b) {
 
 // k rounds of warp argmax over this lane's keys; returns the winners (uniform in the
 // warp). Keys of absent or excluded experts must be passed as absent via `live`.
-__device__ __forceinline__ void warp_topk(const float (&key)[kMaxPerLane], uint32_t live, int k,
+template <int EPL>
+__device__ __forceinline__ void warp_topk(const float (&key)[EPL], uint32_t live, int k,
                                           int lane, int (&sel)[kMaxTopK], float* kth_key) {
   uint32_t taken = 0;
   float last = -INFINITY;
@@ -91,7 +92,7 @@ __device__ __forceinline__ void warp_topk(const float (&key)[kMaxPerLane], uint3
     if (j < k) {
       KeyIdx best{-INFINITY, INT32_MAX};
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
+      for (int i = 0; i < EPL; ++i) {
         const int e = lane + 32 * i;
         if (((live & ~taken) >> i) & 1u && beats(key[i], e, best.key, best.idx)) {
           best.key = key[i];
@@ -108,10 +109,14 @@ __device__ __forceinline__ void warp_topk(const float (&key)[kMaxPerLane], uint3
   if (kth_key) *kth_key = last;
 }
 
+// EPL = experts per lane (lane l holds experts l, l + 32, ...; E <= 32 * EPL).
+// kGrouped: the DeepSeekV3 grouped selection; otherwise the softmax/sigmoid methods.
+template <int EPL, bool kGrouped>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __restrict__ bias,
              int method, int k, int n_group, int topk_group, float rsf,
              int32_t* __restrict__ ids, float* __restrict__ scales) {
+  constexpr int kMaxPerLane = EPL;
   __shared__ float s_key[kRouteWarps][256];
   __shared__ uint8_t s_exact[kRouteWarps][256];
   __shared__ float s_sel_l[kRouteWarps][kMaxTopK];
@@ -122,6 +127,8 @@ route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp;
   const bool valid = t < T;   // warp-uniform; invalid warps still reach the block barriers
+  pdl_trigger();
+  pdl_wait();
 
   if (valid) {
     const float* row = logits + t * E;
@@ -140,7 +147,7 @@ route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __
       key[i] = v;
     }
 
-    if (method == MOE_ROUTE_DEEPSEEKV3) {
+    if (kGrouped) {
       // fp32 approximation of every kappa, and a bound D on |kappa_exact - kappa_approx|:
       // the fp32 sigmoid is within 4e-7 of the true value and both roundings add at most
       // one ulp of the key, so 1e-6 + 2.5e-7 * |kappa| holds with room to spare.
@@ -279,7 +286,7 @@ route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __
     if (tt >= T) continue;
     const double lv = static_cast<double>(s_sel_l[w][j]);
     double e;
-    if (method == MOE_ROUTE_SIGMOID_RENORM || method == MOE_ROUTE_DEEPSEEKV3)
+    if (kGrouped || method == MOE_ROUTE_SIGMOID_RENORM)
       e = sigmoid_d(lv);
     else
       e = exp(lv - static_cast<double>(s_sel_l[w][0]));   // slot 0 holds the largest logit
@@ -295,12 +302,34 @@ route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __
     double wgt;
     if (method == MOE_ROUTE_DEFAULT)
       wgt = s_e[w][j] / s_z[w];
-    else if (method == MOE_ROUTE_DEEPSEEKV3)
+    else if (kGrouped)
       wgt = s_e[w][j] / (s + 1e-20) * static_cast<double>(rsf);
     else
       wgt = s_e[w][j] / s;
     scales[tt * k + j] = __double2float_rn(wgt);
   }
+}
+
+
+template <int EPL, bool kGrouped>
+cudaError_t launch_route_t(const float* logits, int64_t T, const float* bias,
+                           const moe_route_params& p, int32_t* ids, float* scales, cudaStream_t s) {
+  const int64_t blocks = (T + kRouteWarps - 1) / kRouteWarps;
+  return launch_pdl(route_kernel<EPL, kGrouped>, dim3(static_cast<unsigned>(blocks)),
+                    dim3(kRouteWarps * 32), 0, s, logits, T, p.num_experts,
+                    kGrouped ? bias : nullptr, p.method, p.top_k, kGrouped ? p.n_group : 1,
+                    kGrouped ? p.topk_group : 1, kGrouped ? p.routed_scaling_factor : 1.0f, ids,
+                    scales);
+}
+
+template <bool kGrouped>
+cudaError_t launch_route_e(const float* logits, int64_t T, const float* bias,
+                           const moe_route_params& p, int32_t* ids, float* scales, cudaStream_t s) {
+  const int E = p.num_experts;
+  if (E <= 32) return launch_route_t<1, kGrouped>(logits, T, bias, p, ids, scales, s);
+  if (E <= 64) return launch_route_t<2, kGrouped>(logits, T, bias, p, ids, scales, s);
+  if (E <= 128) return launch_route_t<4, kGrouped>(logits, T, bias, p, ids, scales, s);
+  return launch_route_t<8, kGrouped>(logits, T, bias, p, ids, scales, s);
 }
 
 }  // namespace
@@ -309,13 +338,9 @@ moe_status launch_route(const float* logits, int64_t T, const float* bias,
                         const moe_route_params& p, int32_t* ids, float* scales,
                         cudaStream_t s) {
   if (T == 0) return MOE_OK;
-  const int64_t blocks = (T + kRouteWarps - 1) / kRouteWarps;
-  const bool grouped = p.method == MOE_ROUTE_DEEPSEEKV3;
-  route_kernel<<<static_cast<unsigned>(blocks), kRouteWarps * 32, 0, s>>>(
-      logits, T, p.num_experts, grouped ? bias : nullptr, p.method, p.top_k,
-      grouped ? p.n_group : 1, grouped ? p.topk_group : 1,
-      grouped ? p.routed_scaling_factor : 1.0f, ids, scales);
-  cudaError_t err = cudaGetLastError();
+  const cudaError_t err = p.method == MOE_ROUTE_DEEPSEEKV3
+                              ? launch_route_e<true>(logits, T, bias, p, ids, scales, s)
+                              : launch_route_e<false>(logits, T, bias, p, ids, scales, s);
   if (err != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "route_kernel launch: %s", cudaGetErrorString(err));
   return MOE_OK;
