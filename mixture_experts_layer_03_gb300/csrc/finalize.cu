@@ -14,7 +14,6 @@ namespace moe {
 namespace {
 
 constexpr int kFinThreads = 256;
-constexpr int kMaxK = 8;
 
 __device__ __forceinline__ void acc_row(float (&acc)[8], uint4 v, float s) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
@@ -26,12 +25,15 @@ __device__ __forceinline__ void acc_row(float (&acc)[8], uint4 v, float s) {
   }
 }
 
-// One thread per 16-byte vector (8 channels) of one token: its k row loads are issued
-// together, then accumulated in slot order j = 0..k-1 (then the shared row).
+// One thread per 16-byte vector (8 channels) of one token: its K row loads are issued
+// together, then accumulated in slot order j = 0..K-1 (then the shared row).
+template <int K>
 __global__ void __launch_bounds__(kFinThreads)
 finalize_kernel(const __nv_bfloat16* __restrict__ out_perm, const int32_t* __restrict__ perm_inv,
-                const float* __restrict__ scales, int64_t T, int k, int H, int64_t shared_row0,
+                const float* __restrict__ scales, int64_t T, int H, int64_t shared_row0,
                 __nv_bfloat16* __restrict__ y) {
+  constexpr int k = K;
+  constexpr int kMaxK = K;
   pdl_trigger();
   pdl_wait();
   const int nvec = H / 8;
@@ -45,12 +47,8 @@ finalize_kernel(const __nv_bfloat16* __restrict__ out_perm, const int32_t* __res
     float sc[kMaxK];
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
-      row[j] = -1;
-      sc[j] = 0.f;
-      if (j < k) {
-        row[j] = __ldg(perm_inv + t * k + j);
-        sc[j] = __ldg(scales + t * k + j);
-      }
+      row[j] = __ldg(perm_inv + t * k + j);
+      sc[j] = __ldg(scales + t * k + j);
     }
     uint4 val[kMaxK];
 #pragma unroll
@@ -87,20 +85,35 @@ __global__ void cast_kernel(const float* __restrict__ in, __nv_bfloat16* __restr
     out[i] = __float2bfloat16_rn(in[i]);
 }
 
+template <int K>
+cudaError_t launch_finalize_k(const moe_problem& p, const moe_ws_layout& L, const float* scales,
+                              void* y, const char* ws, cudaStream_t s) {
+  const int64_t P = p.T * p.k;
+  const int64_t total = p.T * (p.H / 8);
+  int64_t grid = (total + kFinThreads - 1) / kFinThreads;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 32;
+  if (grid > cap) grid = cap;
+  return launch_pdl(finalize_kernel<K>, dim3(static_cast<unsigned>(grid)), dim3(kFinThreads), 0, s,
+                    reinterpret_cast<const __nv_bfloat16*>(ws + L.out_perm),
+                    reinterpret_cast<const int32_t*>(ws + L.perm_inv), scales, p.T, p.H,
+                    static_cast<int64_t>(p.shared_I > 0 ? P : -1), static_cast<__nv_bfloat16*>(y));
+}
+
 }  // namespace
 
 moe_status launch_finalize(const moe_problem& p, const moe_ws_layout& L, const float* scales,
                            void* y, const char* ws, cudaStream_t s) {
-  const int64_t P = p.T * p.k;
-  const int64_t total = p.T * (p.H / 8);
-  int64_t grid = (total + kFinThreads - 1) / kFinThreads;
-  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
-  if (grid > cap) grid = cap;
-  cudaError_t err = launch_pdl(finalize_kernel, dim3(static_cast<unsigned>(grid)), dim3(kFinThreads), 0, s,
-                               reinterpret_cast<const __nv_bfloat16*>(ws + L.out_perm),
-                               reinterpret_cast<const int32_t*>(ws + L.perm_inv), scales, p.T, p.k, p.H,
-                               static_cast<int64_t>(p.shared_I > 0 ? P : -1),
-                               static_cast<__nv_bfloat16*>(y));
+  cudaError_t err;
+  switch (p.k) {
+    case 1: err = launch_finalize_k<1>(p, L, scales, y, ws, s); break;
+    case 2: err = launch_finalize_k<2>(p, L, scales, y, ws, s); break;
+    case 3: err = launch_finalize_k<3>(p, L, scales, y, ws, s); break;
+    case 4: err = launch_finalize_k<4>(p, L, scales, y, ws, s); break;
+    case 5: err = launch_finalize_k<5>(p, L, scales, y, ws, s); break;
+    case 6: err = launch_finalize_k<6>(p, L, scales, y, ws, s); break;
+    case 7: err = launch_finalize_k<7>(p, L, scales, y, ws, s); break;
+    default: err = launch_finalize_k<8>(p, L, scales, y, ws, s); break;
+  }
   if (err != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "finalize launch: %s", cudaGetErrorString(err));
   return MOE_OK;
