@@ -325,7 +325,7 @@ def run_ours(args, rank, world):
         roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4)}
     roofline.update({"traffic": traffic_record("grouped_gemm.cu", args.workload),
-                     "kernel": "grouped_gemm_kernel<FC1+SwiGLU>",
+                     "kernel": "grouped GEMM FC1+SwiGLU (CTA-pair + single-SM launches)",
                      "peak_source": f"{peak_src} ({'bf16_tflops burst' if tensor_bound else 'hbm_gbs'})",
                      "algorithmic_flops_per_launch": fc1_flops,
                      "algorithmic_bytes_per_launch": fc1_bytes, "ms_per_launch": round(kern_ms["fc1"], 4)})

@@ -93,9 +93,9 @@ bool compute_layout(const moe_problem& p, moe_ws_layout* out) {
   L.counts = o;      o = align_up(o + 4 * size_t(G), A);
   L.starts = o;      o = align_up(o + 4 * size_t(G), A);
   L.offsets = o;     o = align_up(o + 4 * size_t(p.E + 1), A);
-  L.tile_off1 = o;   o = align_up(o + 4 * size_t(G + 1), A);
-  L.tile_off2 = o;   o = align_up(o + 4 * size_t(G + 1), A);
-  L.sched = o;       o = align_up(o + 16, A);
+  L.tile_off1 = o;   o = align_up(o + 8 * size_t(G + 1), A);
+  L.tile_off2 = o;   o = align_up(o + 8 * size_t(G + 1), A);
+  L.sched = o;       o = align_up(o + 32, A);
   L.block_hist = o;  o = align_up(o + 4 * size_t(nb) * size_t(p.E), A);
   L.perm_src = o;    o = align_up(o + 4 * size_t(P), A);
   L.perm_inv = o;    o = align_up(o + 4 * size_t(P), A);

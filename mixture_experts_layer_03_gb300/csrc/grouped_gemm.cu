@@ -1,34 +1,42 @@
-// Steps 3 and 4: grouped GEMM over all experts in one persistent launch.
+// Steps 3 and 4: grouped GEMM over all experts, two persistent launches per GEMM.
 //
-// Scheduling (Dense GEMM -> GroupedGEMM article, section 2.2): tile scheduling over a
-// flattened global tile list rather than one block per expert. The permute step wrote,
+// Scheduling (Dense GEMM -> GroupedGEMM article, section 2.2): tile scheduling over
+// flattened global work lists rather than one block per expert. The permute step wrote,
 // per group g (routed experts, then the optional shared expert), its row count m_g, its
-// first permuted row, and an exclusive scan of its tile counts. Group g contributes
-//     n_mt(g) = floor(m_g / 128) + (m_g % 128 != 0)  row tiles  x  n_nt(g) channel tiles.
-// Row tile mt < floor(m_g/128) is a full 128-row tile computed "token-major":
-//     D[128 tokens, 256] = X[128, K] . W[256, K]^T                  (one UMMA, N = 256)
-// The last, partial row tile (1..127 rows) is computed "weight-major" (swap AB), so a
-// few tokens do not waste a 128-row MMA:
-//     D0[128 ch, n] = W[0:128, K] . X[n, K]^T,  D1[128 ch, n] = W[128:256, K] . X[n, K]^T
-// with n = rows rounded up to 16. Small experts (decode) therefore stream their weights
-// once through MMAs of M = 128 and N = 16..128.
+// first permuted row and exclusive scans of its work. Each group goes to ONE kernel, so
+// the units that share a weight panel run close together in time and reuse it in L2:
 //
-// W rows per tile: FC1 loads gate rows [n0, n0+128) and up rows [I+n0, I+n0+128) of
-// w13[e] (w13 = gate and up merged, vLLM MoE page, section "专家权重如何存储"), so gate
-// channel c and up channel c land in the same TMEM lane (weight-major) or the same
-// thread's columns c and 128+c (token-major); the SwiGLU epilogue h = silu(gate) * up
-// needs no exchange. FC2 loads w2[e] rows [n0, n0+256) (output channels).
+//  * groups with m_g >= 256 -> grouped_gemm_pair_kernel, on 2-CTA clusters with pair
+//    MMAs (tcgen05.mma.cta_group::2, M = 256). Each CTA holds 128 rows of the A operand
+//    and half of the B operand in its own shared memory, so a stage is 32 KB per SM and
+//    six stages fit; each CTA's TMEM receives its 128 rows of the result. A group gives
+//    floor(m_g / 256) token-major units (two full 128-row tiles, one per CTA,
+//        D[256 tokens, 256] = X[256, K] . W[256, K]^T,   A = X, B = W, N = 256)
+//    and one unit for the rows left over: 129..255 rows run token-major with the
+//    missing rows masked; 1..128 rows run weight-major (swap AB,
+//        D[256 weights, n] = W[256, K] . X[n, K]^T,      A = W, B = X,
+//    n = rows rounded up to 16, each CTA holding n/2 token rows), per channel tile.
+//  * groups with m_g < 256 (every decode-sized expert) -> grouped_gemm_kernel, one SM per
+//    tile: a full 128-row tile token-major (D[128, 256] = X . W^T, N = 256) and the
+//    partial tile weight-major (D0[128 ch, n] = W[0:128] . X^T, D1 = W[128:256] . X^T, with
+//    n = rows rounded up to 16); 48 KB stages keep 32 KB of weights per stage in flight,
+//    which is what a weight-streaming (HBM-bound) tile needs.
 //
-// Warp roles (192 threads): warp 0 = TMA producer and tile scheduler, warp 1 = TMEM
-// allocator + MMA issuer, warps 2-5 = epilogue (TMEM lanes 32*(warp%4) .. +31). A 4-stage
-// smem ring (16 KB X + 32 KB W per stage) feeds the MMAs; two 256-column TMEM
-// accumulators let the epilogue of one tile overlap the mainloop of the next.
+// Weight rows (w13 = gate and up merged, vLLM MoE page, section "专家权重如何存储") are
+// arranged so the SwiGLU epilogue (h = silu(gate) * up) finds gate and up of a channel in
+// one thread: token-major tiles load gate rows [n0, n0+128) and up rows [I+n0, I+n0+128)
+// as the two halves of N = 256 (columns c and 128+c); single-SM weight-major tiles load
+// them as D0 and D1 (same TMEM lane); pair weight-major units load, in CTA r, gate rows
+// [n0+64r, +64) and up rows [I+n0+64r, +64) (lanes c and 64+c, swapped through a 4 KB
+// shared buffer). FC2 takes w2[e] rows [n0, n0+256) (output channels).
 //
-// Tiles are claimed dynamically: the producer takes the next index from a global atomic
-// counter and passes it to the MMA and epilogue warps through a small smem ring, so CTAs
-// that run faster (L2 hits, lighter tiles, the nearer die) take more tiles. Claims move
-// through the flattened list in order, so the tiles in flight at any time are neighbours
-// that share weight panels in L2. The last CTA to finish resets the counter.
+// Warp roles (192 threads per CTA): warp 0 = TMA producer (and work claims), warp 1 =
+// TMEM allocator and MMA issuer (in a pair, the first CTA issues), warps 2-5 = epilogue
+// (TMEM lanes 32*(warp%4) .. +31). Two 256-column TMEM accumulators let the epilogue of
+// one unit overlap the next mainloop. Work is claimed dynamically from an atomic counter
+// per list (in a pair, the first CTA claims and passes the index to both CTAs through
+// DSMEM); claims move through the list in order and faster SMs take more work. The last
+// CTA to finish resets the counter.
 //
 // Rows past a group's end inside a tile read the next group's rows (or zero fill past
 // the tensor); they only reach accumulator rows/columns that the epilogue masks.
@@ -47,21 +55,27 @@ namespace {
 
 constexpr int kBK = 64;                              // K elements per stage
 constexpr int kRowBytes = kBK * 2;                   // one K row of a tile = the swizzle width
-constexpr int kStages = 4;
 constexpr int kXStageBytes = 128 * kRowBytes;        // 128 rows of X
-constexpr int kWHalfBytes = 128 * kRowBytes;         // 128 rows of W
-constexpr int kWStageBytes = 2 * kWHalfBytes;
+constexpr int kWStageBytes = 128 * kRowBytes;        // 128 rows of W
+constexpr int kStages = 6;                           // pair kernel: X + W halves, 32 KB
+constexpr int kSingleStages = 4;                     // single kernel: X + 2 W halves, 48 KB
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 512;
 constexpr int kThreads = 192;
 constexpr int kMaxGroups = 257;
-constexpr int kSchedDepth = 4;                       // tile indices in flight inside a CTA
+constexpr int kSchedDepth = 4;                       // work indices in flight inside a CTA
 constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * (kXStageBytes + kWStageBytes);
+constexpr int kSingleSmemBytes = 1024 + kSingleStages * (kXStageBytes + 2 * kWStageBytes);
+constexpr uint16_t kPairMask = 0x3;
+// Consumers that return a scheduling slot to the first CTA: its MMA thread and 4
+// epilogue warps, and the second CTA's producer and 4 epilogue warps.
+constexpr uint32_t kSchedConsumers = 1 + 4 + 1 + 4;
+constexpr int kXchgStride = 17;                      // padded row of the gate/up swap buffer
 
 struct GemmArgs {
   const int32_t* counts;    // [G]
   const int32_t* starts;    // [G]
-  const int32_t* tile_off;  // [G+1]
+  const int32_t* tile_off;  // [G+1] offsets into this kernel's work list
   int32_t G;
   int32_t E;                // routed groups; group E (if G > E) uses the shared maps
   int32_t K_routed, K_shared;
@@ -69,45 +83,84 @@ struct GemmArgs {
   __nv_bfloat16* out;
   int64_t out_ld;
   int32_t* status;
-  int32_t* sched;           // [0] next tile to claim, [1] CTAs finished (both reset to 0 at exit)
+  int32_t* sched;           // [0] next unit to claim, [1] CTAs finished (both reset at exit)
 };
 
-struct Tile {
+struct Unit {
   int g;
-  int token_major;   // 1: 128-row tile, 0: weight-major remainder tile
-  int row0;          // first permuted row
-  int rows;          // valid rows (<= 128)
-  int ntok;          // weight-major: rows rounded up to 16
-  int n0;            // first output channel
+  int token_major;   // 1: two full 128-row tiles; 0: the group's leftover rows, weight-major
+  int row0;          // token-major: this CTA's first row; weight-major: the first leftover row
+  int rows;          // valid rows (token-major 128; weight-major 1..255)
+  int ntok;          // weight-major: rows rounded up to 16 (the MMA N)
+  int n0;            // first output channel of the unit
   int K;
   int N;             // channels of this group
 };
 
-__device__ __forceinline__ Tile decode_tile(int tile, const int32_t* s_off, const int32_t* s_cnt,
-                                            const int32_t* s_start, const GemmArgs& a,
-                                            bool fc1) {
-  // Largest g with tile_off[g] <= tile (groups with no tiles have equal offsets).
-  int lo = 0, hi = a.G - 1;
+// Largest g with off[g] <= idx (groups without work have equal offsets).
+__device__ __forceinline__ int find_group(int idx, const int32_t* s_off, int G) {
+  int lo = 0, hi = G - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (s_off[mid] <= tile) lo = mid; else hi = mid - 1;
+    if (s_off[mid] <= idx) lo = mid; else hi = mid - 1;
   }
-  Tile t;
-  t.g = lo;
-  const int m = s_cnt[lo];
-  const int nfull = m / 128;
-  const int n_mt = nfull + (m % 128 != 0);
-  const int local = tile - s_off[lo];
-  const int nt = local / n_mt;
-  const int mt = local - nt * n_mt;
-  t.token_major = mt < nfull;
-  t.row0 = s_start[lo] + mt * 128;
-  t.rows = min(128, m - mt * 128);
-  t.ntok = (t.rows + 15) & ~15;
-  const bool shared = lo >= a.E;
+  return lo;
+}
+
+__device__ __forceinline__ Unit decode_unit(int unit, const int32_t* s_off, const int32_t* s_cnt,
+                                            const int32_t* s_start, const GemmArgs& a, bool fc1,
+                                            uint32_t rank) {
+  const int g = find_group(unit, s_off, a.G);
+  const int m = s_cnt[g];
+  const int pairs = m >> 8;
+  const int left = m - (pairs << 8);
+  const int nu = pairs + (left > 0);
+  const int local = unit - s_off[g];
+  const int nt = local / nu;
+  const int u = local - nt * nu;
+  const bool shared = g >= a.E;
+  Unit t;
+  t.g = g;
   t.K = shared ? a.K_shared : a.K_routed;
   t.N = shared ? a.N_shared : a.N_routed;
   t.n0 = nt * (fc1 ? kFc1Cols : kFc2Cols);
+  if (u < pairs || left > 128) {
+    // Two row tiles, one per CTA; for the leftover unit (129..255 rows) the second tile
+    // is partial and its missing rows are masked.
+    t.token_major = 1;
+    t.row0 = s_start[g] + 256 * u + 128 * static_cast<int>(rank);
+    t.rows = u < pairs ? 128 : min(128, left - 128 * static_cast<int>(rank));
+    t.ntok = 128;
+  } else {
+    t.token_major = 0;
+    t.row0 = s_start[g] + 256 * pairs;
+    t.rows = left;
+    t.ntok = (left + 15) & ~15;
+  }
+  return t;
+}
+
+// Single-SM list: every row tile of a group with m < 256 (a full tile and/or the partial
+// last tile), channel-tile major.
+__device__ __forceinline__ Unit decode_single(int tile, const int32_t* s_off, const int32_t* s_cnt,
+                                              const int32_t* s_start, const GemmArgs& a, bool fc1) {
+  const int g = find_group(tile, s_off, a.G);
+  const int m = s_cnt[g];
+  const int nfull = m / 128;
+  const int n_mt = nfull + (m % 128 != 0);
+  const int local = tile - s_off[g];
+  const int nt = local / n_mt;
+  const int mt = local - nt * n_mt;
+  const bool shared = g >= a.E;
+  Unit t;
+  t.g = g;
+  t.K = shared ? a.K_shared : a.K_routed;
+  t.N = shared ? a.N_shared : a.N_routed;
+  t.n0 = nt * (fc1 ? kFc1Cols : kFc2Cols);
+  t.token_major = mt < nfull;
+  t.row0 = s_start[g] + mt * 128;
+  t.rows = min(128, m - mt * 128);
+  t.ntok = (t.rows + 15) & ~15;
   return t;
 }
 
@@ -123,6 +176,174 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
+// Token-major epilogue: thread = token row lrow; TMEM columns = channels (FC1: 0..127
+// gate and 128..255 up of channels n0..n0+127; FC2: channels n0..n0+255).
+template <bool kFc1>
+__device__ __forceinline__ void store_token_major(uint32_t tb, const Unit& t, int lrow,
+                                                  const GemmArgs& a) {
+  float va[16], vb[16];
+  const bool valid = lrow < t.rows;
+  __nv_bfloat16* orow = a.out + static_cast<int64_t>(t.row0 + lrow) * a.out_ld;
+  if (kFc1) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < 128; c0 += 16) {
+      tmem_ld2_x16(tb + c0, tb + 128 + c0, va, vb);
+      if (valid && t.n0 + c0 < t.N) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          pk[i] = pack_bf16x2(silu(va[2 * i]) * vb[2 * i], silu(va[2 * i + 1]) * vb[2 * i + 1]);
+        uint4* dst = reinterpret_cast<uint4*>(orow + t.n0 + c0);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int c0 = 0; c0 < 256; c0 += 32) {
+      tmem_ld2_x16(tb + c0, tb + c0 + 16, va, vb);
+      if (valid && t.n0 + c0 < t.N) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          pk[i] = pack_bf16x2(va[2 * i], va[2 * i + 1]);
+          pk[8 + i] = pack_bf16x2(vb[2 * i], vb[2 * i + 1]);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(orow + t.n0 + c0);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+        dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+      }
+    }
+  }
+}
+
+// Weight-major epilogue: TMEM lane = one of this CTA's 128 weight rows, columns = tokens.
+// FC2: lane L is output channel n0 + 128 * rank + L. FC1: lanes 0-63 are the gate and
+// lanes 64-127 the up projection of channels n0 + 64 * rank + (L mod 64); the up half
+// passes through `xchg` to the warps holding the gate half (named barrier 1 over the
+// four epilogue warps).
+template <bool kFc1>
+__device__ __forceinline__ void store_weight_major(uint32_t tb, const Unit& t, int lrow,
+                                                   uint32_t rank, float* xchg,
+                                                   const GemmArgs& a) {
+  float va[16];
+  if (kFc1) {
+    const bool gate_half = lrow < 64;
+    const int c = lrow & 63;
+    const int ch = t.n0 + 64 * static_cast<int>(rank) + c;
+#pragma unroll 1
+    for (int c0 = 0; c0 < t.ntok; c0 += 16) {
+      tmem_ld_x16(tb + c0, va);
+      if (!gate_half) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) xchg[c * kXchgStride + i] = va[i];
+      }
+      named_barrier_sync(1, 128);
+      if (gate_half && ch < t.N) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = c0 + i;
+          if (r < t.rows)
+            a.out[static_cast<int64_t>(t.row0 + r) * a.out_ld + ch] =
+                __float2bfloat16_rn(silu(va[i]) * xchg[c * kXchgStride + i]);
+        }
+      }
+      named_barrier_sync(1, 128);
+    }
+  } else {
+    const int ch = t.n0 + 128 * static_cast<int>(rank) + lrow;
+#pragma unroll 1
+    for (int c0 = 0; c0 < t.ntok; c0 += 16) {
+      tmem_ld_x16(tb + c0, va);
+      if (ch < t.N) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = c0 + i;
+          if (r < t.rows)
+            a.out[static_cast<int64_t>(t.row0 + r) * a.out_ld + ch] = __float2bfloat16_rn(va[i]);
+        }
+      }
+    }
+  }
+}
+
+// Single-SM weight-major epilogue: thread = channel lrow (of the 128 in D0, and of D1);
+// TMEM columns = token rows. FC1: D0 gate, D1 up of the same channel; FC2: D0 channels
+// n0..n0+127, D1 channels n0+128..n0+255.
+template <bool kFc1>
+__device__ __forceinline__ void store_weight_major_single(uint32_t tb, const Unit& t, int lrow,
+                                                          const GemmArgs& a) {
+  float va[16], vb[16];
+  const int ch0 = t.n0 + lrow;
+  const int ch1 = kFc1 ? ch0 : (t.n0 + 128 + lrow);
+  const bool v0 = ch0 < t.N, v1 = ch1 < t.N;
+#pragma unroll 1
+  for (int c0 = 0; c0 < t.ntok; c0 += 16) {
+    tmem_ld2_x16(tb + c0, tb + 128 + c0, va, vb);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int r = c0 + i;
+      if (r < t.rows) {
+        __nv_bfloat16* orow = a.out + static_cast<int64_t>(t.row0 + r) * a.out_ld;
+        if (kFc1) {
+          if (v0) orow[ch0] = __float2bfloat16_rn(silu(va[i]) * vb[i]);
+        } else {
+          if (v0) orow[ch0] = __float2bfloat16_rn(va[i]);
+          if (v1) orow[ch1] = __float2bfloat16_rn(vb[i]);
+        }
+      }
+    }
+  }
+}
+
+// Both kernels: the last CTA to finish resets the work counter for the next launch.
+__device__ __forceinline__ void finish_claims(const GemmArgs& a) {
+  __threadfence();
+  if (atomicAdd(a.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+    atomicExch(a.sched, 0);
+    atomicExch(a.sched + 1, 0);
+  }
+}
+
+// ============================================================== single-SM kernel
+
+// The K loop of one tile of the single-SM kernel. Token-major: A = 128 X rows, B = the
+// 256 W rows of the stage (N = 256). Weight-major: two MMAs, A = each 128-row half of the
+// W stage, B = the tile's X rows (N = ntok), into accumulator columns 0 and 128. One loop
+// per form, as in the pair kernel. Returns false if a stage did not arrive in time.
+template <bool kTokenMajor>
+__device__ __forceinline__ bool single_k_loop(uint32_t d, uint32_t idesc, int nkb, int& stage,
+                                              uint32_t& phase, uint32_t sx0, uint32_t sw0,
+                                              uint64_t* full_bar, uint64_t* empty_bar,
+                                              volatile int* abort) {
+  for (int kb = 0; kb < nkb; ++kb) {
+    if (!mbar_wait(&full_bar[stage], phase, abort)) return false;
+    tc_fence_after();
+    const uint32_t xa = sx0 + stage * kXStageBytes;
+    const uint32_t wa = sw0 + stage * (2 * kWStageBytes);
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk) {
+      const uint32_t accum = (kb | kk) != 0;
+      const uint64_t dx = sdesc_k_major(xa + kk * 32, kRowBytes);
+      if (kTokenMajor) {
+        umma_bf16(d, dx, sdesc_k_major(wa + kk * 32, kRowBytes), idesc, accum);
+      } else {
+        umma_bf16(d, sdesc_k_major(wa + kk * 32, kRowBytes), dx, idesc, accum);
+        umma_bf16(d + 128, sdesc_k_major(wa + kWStageBytes + kk * 32, kRowBytes), dx, idesc,
+                  accum);
+      }
+    }
+    umma_commit(&empty_bar[stage]);
+    if (++stage == kSingleStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+  return true;
+}
+
 template <bool kFc1>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, box 64 x 128
@@ -131,7 +352,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
                     const __grid_constant__ CUtensorMap map_ws,     // shared weights [1, R, K]
                     GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
+  __shared__ uint64_t full_bar[kSingleStages], empty_bar[kSingleStages];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint64_t sched_full[kSchedDepth], sched_empty[kSchedDepth];
   __shared__ int s_tile[kSchedDepth];
@@ -145,12 +366,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
   // 1024-byte aligned stage buffers (the 128-byte swizzle repeats every 1024 bytes).
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint8_t* sX = smem;                                   // kStages x 16 KB
-  uint8_t* sW = smem + kStages * kXStageBytes;          // kStages x 256 W rows
+  uint8_t* sX = smem;                                   // kSingleStages x 16 KB
+  uint8_t* sW = smem + kSingleStages * kXStageBytes;          // kSingleStages x 256 W rows
 
   pdl_trigger();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSingleStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -209,14 +430,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
         s_tile[slot] = tile;
         mbar_arrive(&sched_full[slot]);
         if (tile < 0) break;
-        const Tile t = decode_tile(tile, s_off, s_cnt, s_start, a, kFc1);
+        const Unit t = decode_single(tile, s_off, s_cnt, s_start, a, kFc1);
         const bool shared = t.g >= a.E;
         const CUtensorMap* mw = shared ? &map_ws : &map_w;
         const int ecoord = shared ? 0 : t.g;
         const int wr0 = t.n0;
         const int wr1 = kFc1 ? (t.N + t.n0) : (t.n0 + 128);
         const uint32_t bytes =
-            kWStageBytes + (t.token_major ? kXStageBytes : static_cast<uint32_t>(t.ntok) * kRowBytes);
+            (2 * kWStageBytes) + (t.token_major ? kXStageBytes : static_cast<uint32_t>(t.ntok) * kRowBytes);
         const int nkb = t.K / kBK;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort)) {
@@ -227,7 +448,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
           mbar_arrive_expect_tx(&full_bar[stage], bytes);
           const int kc = kb * kBK;
           uint8_t* xs = sX + stage * kXStageBytes;
-          uint8_t* ws = sW + stage * kWStageBytes;
+          uint8_t* ws = sW + stage * (2 * kWStageBytes);
           if (t.token_major) {
             tma_load_2d(xs, &map_x128, &full_bar[stage], kc, t.row0);
           } else {
@@ -235,9 +456,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
               tma_load_2d(xs + r * kRowBytes, &map_x16, &full_bar[stage], kc, t.row0 + r);
           }
           tma_load_3d(ws, mw, &full_bar[stage], kc, wr0, ecoord);
-          tma_load_3d(ws + kWHalfBytes, mw, &full_bar[stage], kc, wr1, ecoord);
+          tma_load_3d(ws + kWStageBytes, mw, &full_bar[stage], kc, wr1, ecoord);
           ++issued;
-          if (++stage == kStages) {
+          if (++stage == kSingleStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -245,13 +466,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
       }
       if (!ok) {
         // Let the copies already in flight land before the CTA exits: wait (bounded)
-        // on the full barrier of each of the last kStages issues.
+        // on the full barrier of each of the last kSingleStages issues.
         int s = stage;
         uint32_t ph = phase;
-        const int n = issued < kStages ? issued : kStages;
+        const int n = issued < kSingleStages ? issued : kSingleStages;
         for (int i = 0; i < n; ++i) {
           if (--s < 0) {
-            s = kStages - 1;
+            s = kSingleStages - 1;
             ph ^= 1u;
           }
           volatile int never = 0;
@@ -278,7 +499,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
         const int tile = *reinterpret_cast<volatile int*>(&s_tile[slot]);
         mbar_arrive(&sched_empty[slot]);
         if (tile < 0) break;
-        const Tile t = decode_tile(tile, s_off, s_cnt, s_start, a, kFc1);
+        const Unit t = decode_single(tile, s_off, s_cnt, s_start, a, kFc1);
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort)) {
           flag_timeout(a.status, abort);
           ok = false;
@@ -286,36 +507,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
         }
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
-        const uint32_t idesc = t.token_major ? idesc_bf16_f32(128, 256) : idesc_bf16_f32(128, t.ntok);
         const int nkb = t.K / kBK;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, abort)) {
-            flag_timeout(a.status, abort);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t xa = sx0 + stage * kXStageBytes;
-          const uint32_t wa = sw0 + stage * kWStageBytes;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint32_t accum = (kb | kk) != 0;
-            const uint64_t dx = sdesc_k_major(xa + kk * 32, kRowBytes);
-            if (t.token_major) {
-              umma_bf16(d, dx, sdesc_k_major(wa + kk * 32, kRowBytes), idesc, accum);
-            } else {
-              umma_bf16(d, sdesc_k_major(wa + kk * 32, kRowBytes), dx, idesc, accum);
-              umma_bf16(d + 128, sdesc_k_major(wa + kWHalfBytes + kk * 32, kRowBytes), dx, idesc,
-                        accum);
-            }
-          }
-          umma_commit(&empty_bar[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+        ok = t.token_major ? single_k_loop<true>(d, idesc_bf16_f32(128, 256), nkb, stage, phase,
+                                                 sx0, sw0, full_bar, empty_bar, abort)
+                           : single_k_loop<false>(d, idesc_bf16_f32(128, t.ntok), nkb, stage,
+                                                  phase, sx0, sw0, full_bar, empty_bar, abort);
+        if (!ok) {
+          flag_timeout(a.status, abort);
+          break;
         }
-        if (!ok) break;
         umma_commit(&tfull_bar[acc]);
         if (++acc == 2) {
           acc = 0;
@@ -346,7 +546,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
       __syncwarp();
       if (lane == 0) mbar_arrive(&sched_empty[slot]);
       if (tile < 0) break;
-      const Tile t = decode_tile(tile, s_off, s_cnt, s_start, a, kFc1);
+      const Unit t = decode_single(tile, s_off, s_cnt, s_start, a, kFc1);
       const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort);
       // Lanes may leave the poll at different times; tcgen05.ld is warp-collective.
       if (!__all_sync(0xffffffffu, got)) {
@@ -432,15 +632,310 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  if (threadIdx.x == 0) finish_claims(a);
+}
+
+// ============================================================== CTA-pair kernel
+
+// The K loop of one unit, issued by the first CTA's MMA thread: token-major units
+// multiply X rows (A, M = 256 over the pair) by W rows (B, N = 256); weight-major units
+// swap the operands (A = W rows, B = the unit's X rows, N = ntok). A separate loop per
+// form keeps the operand order and the instruction descriptor fixed inside the loop; a
+// per-instruction choice between the two forms cost a quarter of the tensor throughput.
+// Returns false if a stage did not arrive in time.
+template <bool kTokenMajor>
+__device__ __forceinline__ bool pair_k_loop(uint32_t d, uint32_t idesc, int nkb, int& cons,
+                                            uint32_t sx0, uint32_t sw0, uint64_t* full_bar,
+                                            uint64_t* empty_bar, volatile int* abort) {
+  for (int kb = 0; kb < nkb; ++kb) {
+    const int stage = cons % kStages;
+    if (!mbar_wait<true>(&full_bar[stage], (cons / kStages) & 1, abort)) return false;
+    tc_fence_after();
+    const uint32_t xa = sx0 + stage * kXStageBytes;
+    const uint32_t wa = sw0 + stage * kWStageBytes;
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk) {
+      const uint64_t dx = sdesc_k_major(xa + kk * 32, kRowBytes);
+      const uint64_t dw = sdesc_k_major(wa + kk * 32, kRowBytes);
+      if (kTokenMajor) umma_bf16_pair(d, dx, dw, idesc, (kb | kk) != 0);
+      else umma_bf16_pair(d, dw, dx, idesc, (kb | kk) != 0);
+    }
+    // The stage is free in both CTAs once these MMAs have read it.
+    umma_commit_pair(&empty_bar[stage], kPairMask);
+    ++cons;
+  }
+  return true;
+}
+
+template <bool kFc1>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A rows, box 64 x 128
+                    const __grid_constant__ CUtensorMap map_x8,    // A rows, box 64 x 8
+                    const __grid_constant__ CUtensorMap map_w128,  // routed weights, box 64 x 128
+                    const __grid_constant__ CUtensorMap map_ws128, // shared weights, box 64 x 128
+                    const __grid_constant__ CUtensorMap map_w64,   // routed weights, box 64 x 64
+                    const __grid_constant__ CUtensorMap map_ws64,  // shared weights, box 64 x 64
+                    GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
+  __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
+  __shared__ uint64_t sched_full[kSchedDepth], sched_empty[kSchedDepth];
+  __shared__ int s_tile[kSchedDepth];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+  __shared__ int32_t s_off[kMaxGroups + 1], s_cnt[kMaxGroups], s_start[kMaxGroups];
+  __shared__ float s_xchg[64 * kXchgStride];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+  const bool lead = rank == 0;
+
+  // 1024-byte aligned stage buffers (the 128-byte swizzle repeats every 1024 bytes), at
+  // the same offsets in both CTAs: the pair MMA reads the second CTA's operands at the
+  // first CTA's shared-memory addresses.
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint8_t* sX = smem;                                   // kStages x up to 128 X rows
+  uint8_t* sW = smem + kStages * kXStageBytes;          // kStages x 128 W rows
+
+  pdl_trigger();
   if (threadIdx.x == 0) {
-    // Every CTA has claimed its last tile before it gets here; the last one to arrive
-    // resets the counters for the next launch on this workspace.
-    __threadfence();
-    if (atomicAdd(a.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
-      atomicExch(a.sched, 0);
-      atomicExch(a.sched + 1, 0);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);    // first CTA: its producer's arrival + both CTAs' bytes
+      mbar_init(&empty_bar[s], 1);   // the first CTA's pair commit, delivered to both CTAs
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&tfull_bar[s], 1);
+      mbar_init(&tempty_bar[s], 8);  // first CTA: one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(&drain_bar, 1);
+    for (int s = 0; s < kSchedDepth; ++s) {
+      mbar_init(&sched_full[s], 1);
+      mbar_init(&sched_empty[s], kSchedConsumers);   // used in the first CTA only
+    }
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&map_x128);
+    tma_prefetch_map(&map_x8);
+    tma_prefetch_map(&map_w128);
+    tma_prefetch_map(&map_ws128);
+    tma_prefetch_map(&map_w64);
+    tma_prefetch_map(&map_ws64);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&s_tmem_base, kTmemCols);   // collective with the other CTA's warp 1
+    tmem_relinquish_pair();
+  }
+  // Everything above overlaps the previous kernel; the work lists are its output.
+  pdl_wait();
+  for (int i = threadIdx.x; i <= a.G; i += blockDim.x) s_off[i] = a.tile_off[i];
+  for (int i = threadIdx.x; i < a.G; i += blockDim.x) {
+    s_cnt[i] = a.counts[i];
+    s_start[i] = a.starts[i];
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // both CTAs' barriers exist before any remote arrival or copy
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+  volatile int* abort = &s_abort;
+  const int total = s_off[a.G];
+
+  const uint32_t lead_full = mapa_shared(smem_u32(&full_bar[0]), 0);
+  const uint32_t lead_tempty = mapa_shared(smem_u32(&tempty_bar[0]), 0);
+  const uint32_t lead_sched_empty = mapa_shared(smem_u32(&sched_empty[0]), 0);
+  const uint32_t peer_s_tile = mapa_shared(smem_u32(&s_tile[0]), peer);
+  const uint32_t peer_sched_full = mapa_shared(smem_u32(&sched_full[0]), peer);
+  auto release_slot = [&](int slot) {
+    if (lead) mbar_arrive(&sched_empty[slot]);
+    else mbar_arrive_cluster(lead_sched_empty + 8u * slot);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int fills = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int slot = it & (kSchedDepth - 1);
+        const uint32_t sph = (it / kSchedDepth) & 1;
+        int unit;
+        if (lead) {
+          if (!mbar_wait<true>(&sched_empty[slot], sph ^ 1u, abort)) {
+            flag_timeout(a.status, abort);
+            ok = false;
+            break;
+          }
+          unit = atomicAdd(a.sched, 1);
+          if (unit >= total) unit = -1;
+          s_tile[slot] = unit;
+          st_shared_cluster_u32(peer_s_tile + 4u * slot, static_cast<uint32_t>(unit));
+          mbar_arrive(&sched_full[slot]);
+          mbar_arrive_cluster(peer_sched_full + 8u * slot);
+        } else {
+          if (!mbar_wait<true>(&sched_full[slot], sph, abort)) {
+            flag_timeout(a.status, abort);
+            ok = false;
+            break;
+          }
+          unit = *reinterpret_cast<volatile int*>(&s_tile[slot]);
+          release_slot(slot);
+        }
+        if (unit < 0) break;
+        const Unit t = decode_unit(unit, s_off, s_cnt, s_start, a, kFc1, rank);
+        const bool shared = t.g >= a.E;
+        const CUtensorMap* mw128 = shared ? &map_ws128 : &map_w128;
+        const CUtensorMap* mw64 = shared ? &map_ws64 : &map_w64;
+        const int ecoord = shared ? 0 : t.g;
+        const int r = static_cast<int>(rank);
+        // This CTA's token rows and its share of the weight rows.
+        const int half = t.ntok >> 1;
+        const int xrow = t.token_major ? t.row0 : t.row0 + r * half;
+        // Weight-major units have at most 128 token rows: each CTA loads its <= 64 rows in
+        // 8-row boxes (the same byte count in both CTAs).
+        const uint32_t xbytes = t.token_major ? kXStageBytes : static_cast<uint32_t>(half) * kRowBytes;
+        const uint32_t tx_bytes = 2u * (xbytes + kWStageBytes);
+        const int nkb = t.K / kBK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int stage = fills % kStages;
+          if (!mbar_wait<true>(&empty_bar[stage], ((fills / kStages) & 1) ^ 1u, abort)) {
+            flag_timeout(a.status, abort);
+            ok = false;
+            break;
+          }
+          if (lead) mbar_arrive_expect_tx(&full_bar[stage], tx_bytes);
+          const int kc = kb * kBK;
+          const uint32_t fb = lead_full + 8u * stage;
+          uint8_t* xs = sX + stage * kXStageBytes;
+          uint8_t* wsm = sW + stage * kWStageBytes;
+          if (t.token_major) {
+            tma_load_2d_pair(xs, &map_x128, fb, kc, xrow);
+            const int wrow = kFc1 ? (lead ? t.n0 : t.N + t.n0) : (t.n0 + 128 * r);
+            tma_load_3d_pair(wsm, mw128, fb, kc, wrow, ecoord);
+          } else {
+            for (int q = 0; q < half; q += 8)
+              tma_load_2d_pair(xs + q * kRowBytes, &map_x8, fb, kc, xrow + q);
+            if (kFc1) {
+              tma_load_3d_pair(wsm, mw64, fb, kc, t.n0 + 64 * r, ecoord);
+              tma_load_3d_pair(wsm + 64 * kRowBytes, mw64, fb, kc, t.N + t.n0 + 64 * r, ecoord);
+            } else {
+              tma_load_3d_pair(wsm, mw128, fb, kc, t.n0 + 128 * r, ecoord);
+            }
+          }
+          ++fills;
+        }
+      }
+      // Before this CTA may exit, the first CTA's commits for every stage it filled must
+      // have arrived (they target this CTA's barriers); bounded.
+      volatile int never = 0;
+      const int first = fills > kStages ? fills - kStages : 0;
+      for (int f = first; f < fills; ++f)
+        mbar_wait<true>(&empty_bar[f % kStages], (f / kStages) & 1, &never);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && lead) {
+      // ------------------------------------------------------------ MMA issuer (first CTA)
+      int cons = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      const uint32_t sx0 = smem_u32(sX), sw0 = smem_u32(sW);
+      for (int it = 0; ok; ++it) {
+        const int slot = it & (kSchedDepth - 1);
+        if (!mbar_wait<true>(&sched_full[slot], (it / kSchedDepth) & 1, abort)) {
+          flag_timeout(a.status, abort);
+          ok = false;
+          break;
+        }
+        const int unit = *reinterpret_cast<volatile int*>(&s_tile[slot]);
+        release_slot(slot);
+        if (unit < 0) break;
+        const Unit t = decode_unit(unit, s_off, s_cnt, s_start, a, kFc1, 0);
+        if (!mbar_wait<true>(&tempty_bar[acc], acc_phase ^ 1u, abort)) {
+          flag_timeout(a.status, abort);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+        const int nkb = t.K / kBK;
+        ok = t.token_major
+                 ? pair_k_loop<true>(d, idesc_bf16_f32(256, 256), nkb, cons, sx0, sw0, full_bar,
+                                     empty_bar, abort)
+                 : pair_k_loop<false>(d, idesc_bf16_f32(256, t.ntok), nkb, cons, sx0, sw0,
+                                      full_bar, empty_bar, abort);
+        if (!ok) {
+          flag_timeout(a.status, abort);
+          break;
+        }
+        umma_commit_pair(&tfull_bar[acc], kPairMask);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // Wait (bounded) for every MMA issued so far before TMEM is released.
+        umma_commit_pair(&drain_bar, 0x1);
+        volatile int never = 0;
+        mbar_wait(&drain_bar, 0, &never);
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int lrow = q * 32 + lane;         // accumulator row (lane) of this thread
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int it = 0;; ++it) {
+      const int slot = it & (kSchedDepth - 1);
+      const bool have = mbar_wait<true>(&sched_full[slot], (it / kSchedDepth) & 1, abort);
+      if (!__all_sync(0xffffffffu, have)) {
+        flag_timeout(a.status, abort);
+        break;
+      }
+      const int unit = *reinterpret_cast<volatile int*>(&s_tile[slot]);
+      __syncwarp();
+      if (lane == 0) release_slot(slot);
+      if (unit < 0) break;
+      const Unit t = decode_unit(unit, s_off, s_cnt, s_start, a, kFc1, rank);
+      const bool got = mbar_wait<true>(&tfull_bar[acc], acc_phase, abort);
+      // Lanes may leave the poll at different times; tcgen05.ld is warp-collective.
+      if (!__all_sync(0xffffffffu, got)) {
+        flag_timeout(a.status, abort);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * kAccCols) +
+                          (static_cast<uint32_t>(q * 32) << 16);
+      if (t.token_major) store_token_major<kFc1>(tb, t, lrow, a);
+      else store_weight_major<kFc1>(tb, t, lrow, rank, s_xchg, a);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (lead) mbar_arrive(&tempty_bar[acc]);
+        else mbar_arrive_cluster(lead_tempty + 8u * acc);
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
   }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);   // collective with the other CTA's warp 1
+  }
+  // No CTA leaves while the other may still write into it or arrive on its barriers.
+  cluster_sync();
+  if (threadIdx.x == 0) finish_claims(a);
 }
 
 // ---------------------------------------------------------------- host side
@@ -466,7 +961,7 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// bf16 matrix [rows, cols] (cols contiguous), box = 64 cols x box_rows rows.
+// bf16 matrix [rows, cols] (cols contiguous), box = kBK cols x box_rows rows.
 bool encode_map2(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows) {
   EncodeTiledFn enc = get_encode_fn();
@@ -481,7 +976,7 @@ bool encode_map2(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
   return r == CUDA_SUCCESS;
 }
 
-// bf16 tensor [planes, rows, cols] (cols contiguous), box = 64 cols x box_rows rows x 1.
+// bf16 tensor [planes, rows, cols] (cols contiguous), box = kBK cols x box_rows rows x 1.
 bool encode_map3(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t cols,
                  uint32_t box_rows) {
   EncodeTiledFn enc = get_encode_fn();
@@ -496,48 +991,68 @@ bool encode_map3(CUtensorMap* m, const void* base, uint64_t planes, uint64_t row
   return r == CUDA_SUCCESS;
 }
 
+// Per device: the large dynamic shared memory opt-in of both kernels, and how many 2-CTA
+// clusters of the pair kernel can be resident at once.
 template <bool kFc1>
-moe_status prepare_kernel() {
-  static int done_dev[64] = {0};
+moe_status prepare_kernels(int* max_clusters) {
+  static int clusters_dev[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
     return set_error(MOE_ERR_CUDA, "cudaGetDevice failed");
-  if (!done_dev[dev]) {
+  if (!clusters_dev[dev]) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kFc1>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSingleSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kFc1>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    done_dev[dev] = 1;
+    const int sms = device_sm_count();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<kFc1>, &cfg) != cudaSuccess ||
+        n < 1) {
+      cudaGetLastError();   // clear the failed query; fall back to one cluster per SM pair
+      n = sms / 2;
+    }
+    clusters_dev[dev] = n;
   }
+  *max_clusters = clusters_dev[dev];
   return MOE_OK;
 }
 
 template <bool kFc1>
 moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void* w,
                        const void* w_s, char* ws, cudaStream_t s) {
-  moe_status st = prepare_kernel<kFc1>();
+  int max_clusters = 1;
+  moe_status st = prepare_kernels<kFc1>(&max_clusters);
   if (st != MOE_OK) return st;
   const int64_t R = L.rows;
   const int has_shared = p.shared_I > 0;
-  CUtensorMap mx128, mx16, mw, mws;
+  CUtensorMap mx128, mx8, mx16, mw128, mws128, mw64, mws64;
   const void* A = kFc1 ? static_cast<const void*>(ws + L.x_perm) : static_cast<const void*>(ws + L.h);
   const uint64_t a_cols = kFc1 ? static_cast<uint64_t>(p.H) : static_cast<uint64_t>(L.h_ld);
-  bool ok = encode_map2(&mx128, A, R, a_cols, 128) && encode_map2(&mx16, A, R, a_cols, 16);
-  if (kFc1) {
-    ok = ok && encode_map3(&mw, w, p.E, 2ull * p.I, p.H, 128);
-    ok = ok && (has_shared ? encode_map3(&mws, w_s, 1, 2ull * p.shared_I, p.H, 128)
-                           : encode_map3(&mws, w, p.E, 2ull * p.I, p.H, 128));
-  } else {
-    ok = ok && encode_map3(&mw, w, p.E, p.H, p.I, 128);
-    ok = ok && (has_shared ? encode_map3(&mws, w_s, 1, p.H, p.shared_I, 128)
-                           : encode_map3(&mws, w, p.E, p.H, p.I, 128));
-  }
+  bool ok = encode_map2(&mx128, A, R, a_cols, 128) && encode_map2(&mx8, A, R, a_cols, 8) &&
+            encode_map2(&mx16, A, R, a_cols, 16);
+  // Weights [planes, rows, K]: FC1 w13 [E, 2I, H] (shared [1, 2Is, H]); FC2 w2 [E, H, I]
+  // (shared [1, H, Is]).
+  const uint64_t wr = kFc1 ? 2ull * p.I : static_cast<uint64_t>(p.H);
+  const uint64_t wk = kFc1 ? static_cast<uint64_t>(p.H) : static_cast<uint64_t>(p.I);
+  const uint64_t sr = kFc1 ? 2ull * p.shared_I : static_cast<uint64_t>(p.H);
+  const uint64_t sk = kFc1 ? static_cast<uint64_t>(p.H) : static_cast<uint64_t>(p.shared_I);
+  ok = ok && encode_map3(&mw128, w, p.E, wr, wk, 128) && encode_map3(&mw64, w, p.E, wr, wk, 64);
+  if (has_shared)
+    ok = ok && encode_map3(&mws128, w_s, 1, sr, sk, 128) && encode_map3(&mws64, w_s, 1, sr, sk, 64);
+  else
+    ok = ok && encode_map3(&mws128, w, p.E, wr, wk, 128) && encode_map3(&mws64, w, p.E, wr, wk, 64);
   if (!ok) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
   GemmArgs a;
   a.counts = reinterpret_cast<const int32_t*>(ws + L.counts);
   a.starts = reinterpret_cast<const int32_t*>(ws + L.starts);
-  a.tile_off = reinterpret_cast<const int32_t*>(ws + (kFc1 ? L.tile_off1 : L.tile_off2));
   a.G = L.groups;
   a.E = p.E;
   if (kFc1) {
@@ -556,18 +1071,41 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
     a.out_ld = p.H;
   }
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
-  a.sched = reinterpret_cast<int32_t*>(ws + L.sched) + (kFc1 ? 0 : 2);
+  // Work lists [pair units | single-SM tiles], each G+1 offsets; counters [pair | single].
+  const int32_t* lists = reinterpret_cast<const int32_t*>(ws + (kFc1 ? L.tile_off1 : L.tile_off2));
+  int32_t* sched = reinterpret_cast<int32_t*>(ws + L.sched) + (kFc1 ? 0 : 4);
 
-  // Upper bound on the device-side tile count: each group has at most
-  // floor(m/128) + 1 row tiles.
+  // Upper bounds on the device-side work per channel tile: the pair units of all groups
+  // together are at most R/256 + (groups of >= 256 rows, at most R/256); with the pair
+  // kernel in use a single-SM group has at most 2 row tiles, without it at most
+  // m/128 + 1 (R/128 + G over all groups).
   const int nI = has_shared && p.shared_I > p.I ? p.shared_I : p.I;
   const int64_t n_nt = kFc1 ? (nI + kFc1Cols - 1) / kFc1Cols : (p.H + kFc2Cols - 1) / kFc2Cols;
-  const int64_t bound = ((R + 127) / 128 + L.groups) * n_nt;
-  int64_t grid = device_sm_count();
-  if (grid > bound) grid = bound;
-  if (grid < 1) grid = 1;
-  cudaError_t err = launch_pdl(grouped_gemm_kernel<kFc1>, dim3(static_cast<unsigned>(grid)),
-                               dim3(kThreads), kSmemBytes, s, mx128, mx16, mw, mws, a);
+  const bool use_pairs = pair_min_rows(p) <= 2 * kTileRows;
+  const int64_t pair_bound = use_pairs ? 2 * (R / 256) * n_nt : 0;
+  const int64_t single_bound =
+      (use_pairs ? 2 * static_cast<int64_t>(L.groups) : R / kTileRows + L.groups) * n_nt;
+
+  cudaError_t err = cudaSuccess;
+  {
+    GemmArgs as = a;
+    as.tile_off = lists + (L.groups + 1);
+    as.sched = sched + 2;
+    int64_t grid = device_sm_count();
+    if (grid > single_bound) grid = single_bound;
+    if (grid < 1) grid = 1;
+    err = launch_pdl(grouped_gemm_kernel<kFc1>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
+                     kSingleSmemBytes, s, mx128, mx16, mw128, mws128, as);
+  }
+  if (err == cudaSuccess && pair_bound > 0) {
+    GemmArgs ap = a;
+    ap.tile_off = lists;
+    ap.sched = sched;
+    int64_t clusters = max_clusters;
+    if (clusters > pair_bound) clusters = pair_bound;
+    err = launch_pdl(grouped_gemm_pair_kernel<kFc1>, dim3(static_cast<unsigned>(2 * clusters)),
+                     dim3(kThreads), kSmemBytes, s, mx128, mx8, mw128, mws128, mw64, mws64, ap);
+  }
   if (err != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "grouped_gemm launch: %s", cudaGetErrorString(err));
   return MOE_OK;

@@ -18,6 +18,14 @@ constexpr int kTileRows = 128;    // token rows of a full (token-major) tile
 constexpr int kFc1Cols = 128;     // FC1 output channels per tile (gate and up each)
 constexpr int kFc2Cols = 256;     // FC2 output channels per tile
 
+// Groups of at least this many rows are tiled by the CTA-pair GEMM kernel, smaller ones
+// by the single-SM kernel. The pair kernel is used only when the routed groups average at
+// least one full row tile (T * k >= 128 * E); otherwise every group, of any size, goes to
+// the single-SM kernel and the pair kernel is not launched.
+inline int pair_min_rows(const moe_problem& p) {
+  return p.T * p.k >= static_cast<int64_t>(kTileRows) * p.E ? 2 * kTileRows : INT32_MAX;
+}
+
 // Fills the layout; returns false when the problem is outside the envelope.
 bool compute_layout(const moe_problem& p, moe_ws_layout* out);
 

@@ -86,16 +86,17 @@ struct PlanArgs {
   int I;
   int shared_I;
   int H;
+  int pair_min_rows;   // groups with at least this many rows go to the CTA-pair list
   const int32_t* block_hist;
   int32_t* counts;     // [G]
   int32_t* starts;     // [G]
   int32_t* offsets;    // [E+1]
-  int32_t* tile_off1;  // [G+1]
-  int32_t* tile_off2;  // [G+1]
+  int32_t* tile_off1;  // [2][G+1]: FC1 offsets into the pair list, then the single-SM list
+  int32_t* tile_off2;  // [2][G+1]: FC2 offsets into the pair list, then the single-SM list
   int32_t* perm_src;   // [P]
   int32_t* perm_inv;   // [P]
   int32_t* status;
-  int32_t* sched;      // [4] grouped-GEMM tile counters, zeroed here every forward
+  int32_t* sched;      // [8] grouped-GEMM work counters, zeroed here every forward
 };
 
 // kSingleChunk: the whole problem is one chunk (one block); the block counts its own
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
     // starting at P). Tiles per group: full 128-row tiles plus one remainder tile, times
     // the output-channel tiles of the GEMM.
     const int G = E + a.has_shared;
-    int cnt = 0, start = 0, n1 = 0, n2 = 0;
+    int cnt = 0, start = 0, np1 = 0, ns1 = 0, np2 = 0, ns2 = 0;
     if (tid < E) {
       cnt = tot;
       start = off;
@@ -154,23 +155,41 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
     if (tid < G) {
       a.counts[tid] = cnt;
       a.starts[tid] = start;
-      const int mt = cnt / kTileRows + (cnt % kTileRows != 0);
+      // Work of the grouped GEMM, per output-channel tile. A group of >= pair_min_rows
+      // (256) rows goes to the CTA-pair kernel: floor(m / 256) units of two full 128-row
+      // tiles plus one unit for the rows left over. Any other group goes to the single-SM
+      // kernel: one tile per 128 rows (full tiles and/or the partial last one).
       const int nI = (tid < E) ? a.I : a.shared_I;
-      n1 = mt * ((nI + kFc1Cols - 1) / kFc1Cols);
-      n2 = mt * ((a.H + kFc2Cols - 1) / kFc2Cols);
+      const int c1 = (nI + kFc1Cols - 1) / kFc1Cols;
+      const int c2 = (a.H + kFc2Cols - 1) / kFc2Cols;
+      if (cnt >= a.pair_min_rows) {
+        const int units = (cnt >> 8) + ((cnt & 255) != 0);
+        np1 = units * c1;
+        np2 = units * c2;
+      } else {
+        const int tiles = cnt / kTileRows + (cnt % kTileRows != 0);
+        ns1 = tiles * c1;
+        ns2 = tiles * c2;
+      }
     }
-    int tot1 = 0, tot2 = 0;
-    const int o1 = block_exclusive_scan(n1, G, s_warp, &tot1);
-    const int o2 = block_exclusive_scan(n2, G, s_warp, &tot2);
+    int t_p1 = 0, t_s1 = 0, t_p2 = 0, t_s2 = 0;
+    const int o_p1 = block_exclusive_scan(np1, G, s_warp, &t_p1);
+    const int o_s1 = block_exclusive_scan(ns1, G, s_warp, &t_s1);
+    const int o_p2 = block_exclusive_scan(np2, G, s_warp, &t_p2);
+    const int o_s2 = block_exclusive_scan(ns2, G, s_warp, &t_s2);
     if (tid < G) {
-      a.tile_off1[tid] = o1;
-      a.tile_off2[tid] = o2;
+      a.tile_off1[tid] = o_p1;
+      a.tile_off1[G + 1 + tid] = o_s1;
+      a.tile_off2[tid] = o_p2;
+      a.tile_off2[G + 1 + tid] = o_s2;
     }
     if (tid == 0) {
-      a.tile_off1[G] = tot1;
-      a.tile_off2[G] = tot2;
+      a.tile_off1[G] = t_p1;
+      a.tile_off1[2 * G + 1] = t_s1;
+      a.tile_off2[G] = t_p2;
+      a.tile_off2[2 * G + 1] = t_s2;
     }
-    if (tid < 4) a.sched[tid] = 0;
+    if (tid < 8) a.sched[tid] = 0;
   }
   __syncthreads();
 
@@ -255,6 +274,7 @@ moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const vo
   a.I = p.I;
   a.shared_I = p.shared_I;
   a.H = p.H;
+  a.pair_min_rows = pair_min_rows(p);
   a.block_hist = reinterpret_cast<const int32_t*>(ws + L.block_hist);
   a.counts = reinterpret_cast<int32_t*>(ws + L.counts);
   a.starts = reinterpret_cast<int32_t*>(ws + L.starts);

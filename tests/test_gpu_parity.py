@@ -122,12 +122,17 @@ def test_permute_parity(moe, T, E, k):
     assert np.array_equal(ws.region("perm_inv", P, torch.int32).cpu().numpy(), perm_inv)
     xp = ws.region("x_perm", P * H, torch.bfloat16).view(P, H).cpu()
     assert torch.equal(xp, x[torch.from_numpy(perm_src).long() // k])
-    # tile lists: per group floor(m/128) + (m%128 > 0) row tiles x channel tiles
-    mt = counts // 128 + (counts % 128 > 0)
-    t1 = ws.region("tile_off1", E + 1, torch.int32).cpu().numpy()
-    t2 = ws.region("tile_off2", E + 1, torch.int32).cpu().numpy()
-    assert np.array_equal(t1, np.concatenate([[0], np.cumsum(mt * 1)]))
-    assert np.array_equal(t2, np.concatenate([[0], np.cumsum(mt * 1)]))
+    # work lists (one channel tile each here: I = 64, H = 128). The CTA-pair kernel is in
+    # use when T * k >= 128 * E; then a group of >= 256 rows has floor(m / 256) +
+    # (m % 256 > 0) units in the CTA-pair list. Every other group has ceil(m / 128)
+    # tiles in the single-SM list.
+    big = (counts >= 256) & (T * k >= 128 * E)
+    pair_units = np.where(big, counts // 256 + (counts % 256 > 0), 0)
+    single_tiles = np.where(big, 0, counts // 128 + (counts % 128 > 0))
+    for name in ("tile_off1", "tile_off2"):
+        lst = ws.region(name, 2 * (E + 1), torch.int32).cpu().numpy()
+        assert np.array_equal(lst[:E + 1], np.concatenate([[0], np.cumsum(pair_units)]))
+        assert np.array_equal(lst[E + 1:], np.concatenate([[0], np.cumsum(single_tiles)]))
     st, flags = moe.moe_read_device_status(ws)
     assert st == moe.MOE_OK and flags == 0
 
@@ -183,6 +188,9 @@ SMALL_CASES = [
     (300, 256, 192, 8, 2, 0, "route"),         # weight-major tiles, ragged FC1 channel tile
     (700, 384, 320, 4, 2, 0, "route"),         # token-major + remainder tiles, ragged FC2 tile
     (1000, 256, 256, 8, 1, 0, "one_expert"),   # one expert holds every row (7 full tiles + 104)
+    (1100, 256, 256, 8, 1, 0, "one_expert"),   # CTA pairs: 4 units + 76 rows (weight-major)
+    (1200, 384, 320, 8, 1, 0, "one_expert"),   # CTA pairs: 4 units + 176 rows (masked pair)
+    (2200, 256, 192, 4, 2, 256, "route"),      # CTA pairs for routed and shared groups
     (513, 128, 128, 8, 8, 0, "route"),         # k = E: every expert every token
     (200, 192, 128, 16, 4, 128, "random_dup"), # repeated ids in a row, shared expert
     (130, 128, 64, 1, 1, 0, "route"),          # E = 1, k = 1: the dense FFN (128 + 2 rows)
