@@ -211,11 +211,10 @@ def run_ours(args, rank, world):
         moe.moe_route(lg, w.method, w.k, stream=s, **route_kw)
         moe.moe_forward(xx, ids, sc, w13, w2, w13s, w2s, y=y, workspace=ws, stream=s)
 
-    # route; permute (the histogram kernel only with more than one 4096-pair chunk, the
-    # plan kernel, the row gather); FC1 and FC2 (single-SM kernel, plus the CTA-pair
-    # kernel when T*k >= 128*E); finalize
-    gemm_launches = 2 if w.T * w.k >= 128 * w.E else 1
-    launches_per_step = 1 + (3 if ws.layout["n_chunks"] > 1 else 2) + 2 * gemm_launches + 1
+    # route; permute (the histogram kernel only with more than one 1024-pair chunk, the
+    # plan kernel, the row gather); FC1 and FC2 (the CTA-pair kernel when T*k >= 128*E,
+    # else the single-SM kernel); finalize
+    launches_per_step = 1 + (3 if ws.layout["n_chunks"] > 1 else 2) + 2 + 1
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()

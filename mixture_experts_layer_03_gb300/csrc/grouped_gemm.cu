@@ -1075,19 +1075,17 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
   const int32_t* lists = reinterpret_cast<const int32_t*>(ws + (kFc1 ? L.tile_off1 : L.tile_off2));
   int32_t* sched = reinterpret_cast<int32_t*>(ws + L.sched) + (kFc1 ? 0 : 4);
 
-  // Upper bounds on the device-side work per channel tile: the pair units of all groups
-  // together are at most R/256 + (groups of >= 256 rows, at most R/256); with the pair
-  // kernel in use a single-SM group has at most 2 row tiles, without it at most
-  // m/128 + 1 (R/128 + G over all groups).
+  // One of the two kernels takes every group (see pair_min_rows). Upper bounds on its
+  // work per channel tile: pair units at most R/256 + G, single-SM tiles at most
+  // R/128 + G.
   const int nI = has_shared && p.shared_I > p.I ? p.shared_I : p.I;
   const int64_t n_nt = kFc1 ? (nI + kFc1Cols - 1) / kFc1Cols : (p.H + kFc2Cols - 1) / kFc2Cols;
   const bool use_pairs = pair_min_rows(p) <= 2 * kTileRows;
-  const int64_t pair_bound = use_pairs ? 2 * (R / 256) * n_nt : 0;
-  const int64_t single_bound =
-      (use_pairs ? 2 * static_cast<int64_t>(L.groups) : R / kTileRows + L.groups) * n_nt;
+  const int64_t pair_bound = use_pairs ? (R / 256 + L.groups) * n_nt : 0;
+  const int64_t single_bound = use_pairs ? 0 : (R / kTileRows + L.groups) * n_nt;
 
   cudaError_t err = cudaSuccess;
-  {
+  if (single_bound > 0) {
     GemmArgs as = a;
     as.tile_off = lists + (L.groups + 1);
     as.sched = sched + 2;

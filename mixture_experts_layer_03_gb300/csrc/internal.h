@@ -10,7 +10,7 @@
 namespace moe {
 
 // Permute: one block handles a chunk of this many (token, slot) pairs.
-constexpr int kPermChunk = 4096;
+constexpr int kPermChunk = 1024;
 constexpr int kPermThreads = 512;
 
 // Grouped GEMM tiling.
@@ -18,12 +18,13 @@ constexpr int kTileRows = 128;    // token rows of a full (token-major) tile
 constexpr int kFc1Cols = 128;     // FC1 output channels per tile (gate and up each)
 constexpr int kFc2Cols = 256;     // FC2 output channels per tile
 
-// Groups of at least this many rows are tiled by the CTA-pair GEMM kernel, smaller ones
-// by the single-SM kernel. The pair kernel is used only when the routed groups average at
-// least one full row tile (T * k >= 128 * E); otherwise every group, of any size, goes to
-// the single-SM kernel and the pair kernel is not launched.
+// Which GEMM kernel tiles the groups. When the routed groups average at least one full
+// row tile (T * k >= 128 * E), the CTA-pair kernel takes every group (groups of fewer
+// than 256 rows become its masked or weight-major units) and the single-SM kernel is not
+// launched; otherwise every group goes to the single-SM kernel and the pair kernel is not
+// launched. Returns the fewest rows of a group in the pair kernel's list.
 inline int pair_min_rows(const moe_problem& p) {
-  return p.T * p.k >= static_cast<int64_t>(kTileRows) * p.E ? 2 * kTileRows : INT32_MAX;
+  return p.T * p.k >= static_cast<int64_t>(kTileRows) * p.E ? 1 : INT32_MAX;
 }
 
 // Fills the layout; returns false when the problem is outside the envelope.

@@ -156,8 +156,8 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
       a.counts[tid] = cnt;
       a.starts[tid] = start;
       // Work of the grouped GEMM, per output-channel tile. A group of >= pair_min_rows
-      // (256) rows goes to the CTA-pair kernel: floor(m / 256) units of two full 128-row
-      // tiles plus one unit for the rows left over. Any other group goes to the single-SM
+      // rows goes to the CTA-pair kernel: floor(m / 256) units of two full 128-row tiles
+      // plus one unit for the rows left over. Any other group goes to the single-SM
       // kernel: one tile per 128 rows (full tiles and/or the partial last one).
       const int nI = (tid < E) ? a.I : a.shared_I;
       const int c1 = (nI + kFc1Cols - 1) / kFc1Cols;
@@ -253,7 +253,17 @@ gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ p
     }
     const uint4* s = reinterpret_cast<const uint4*>(x + src * H);
     uint4* d = reinterpret_cast<uint4*>(x_perm + r * H);
-    for (int v = lane; v < nvec; v += 32) d[v] = __ldg(s + v);
+    // Four independent 16-byte loads in flight per lane before their stores.
+    int v = lane;
+    for (; v + 96 < nvec; v += 128) {
+      const uint4 a0 = __ldg(s + v), a1 = __ldg(s + v + 32), a2 = __ldg(s + v + 64),
+                  a3 = __ldg(s + v + 96);
+      d[v] = a0;
+      d[v + 32] = a1;
+      d[v + 64] = a2;
+      d[v + 96] = a3;
+    }
+    for (; v < nvec; v += 32) d[v] = __ldg(s + v);
   }
 }
 

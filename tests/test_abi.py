@@ -74,7 +74,7 @@ def test_workspace_layout(moe):
     p = moe.make_problem(T=512, H=7168, I=2048, E=256, k=8, shared_I=2048)
     L = moe.moe_workspace_layout(p)
     P, R = 512 * 8, 512 * 8 + 512
-    assert L["rows"] == R and L["groups"] == 257 and L["h_ld"] == 2048 and L["n_chunks"] == 1
+    assert L["rows"] == R and L["groups"] == 257 and L["h_ld"] == 2048 and L["n_chunks"] == 4
     names = ["status", "counts", "starts", "offsets", "tile_off1", "tile_off2", "sched", "block_hist",
              "perm_src", "perm_inv", "x_perm", "h", "out_perm", "total"]
     offs = [L[n] for n in names]

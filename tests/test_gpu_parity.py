@@ -103,7 +103,7 @@ def test_route_nonfinite_logits_never_beat_finite(moe):
 
 # ------------------------------------------------------------------------ permute
 
-@pytest.mark.parametrize("T,E,k", [(300, 8, 2), (5000, 64, 4), (1, 4, 1), (2048, 256, 8),
+@pytest.mark.parametrize("T,E,k", [(300, 8, 2), (5000, 64, 4), (1, 4, 1), (2048, 256, 8), (513, 16, 2),
                                    (9000, 3, 3)])
 def test_permute_parity(moe, T, E, k):
     g = torch.Generator().manual_seed(T + E)
@@ -122,11 +122,10 @@ def test_permute_parity(moe, T, E, k):
     assert np.array_equal(ws.region("perm_inv", P, torch.int32).cpu().numpy(), perm_inv)
     xp = ws.region("x_perm", P * H, torch.bfloat16).view(P, H).cpu()
     assert torch.equal(xp, x[torch.from_numpy(perm_src).long() // k])
-    # work lists (one channel tile each here: I = 64, H = 128). The CTA-pair kernel is in
-    # use when T * k >= 128 * E; then a group of >= 256 rows has floor(m / 256) +
-    # (m % 256 > 0) units in the CTA-pair list. Every other group has ceil(m / 128)
-    # tiles in the single-SM list.
-    big = (counts >= 256) & (T * k >= 128 * E)
+    # work lists (one channel tile each here: I = 64, H = 128). When T * k >= 128 * E the
+    # CTA-pair kernel takes every group: floor(m / 256) + (m % 256 > 0) units each.
+    # Otherwise every group has ceil(m / 128) tiles in the single-SM list.
+    big = (counts >= 1) & (T * k >= 128 * E)
     pair_units = np.where(big, counts // 256 + (counts % 256 > 0), 0)
     single_tiles = np.where(big, 0, counts // 128 + (counts % 128 > 0))
     for name in ("tile_off1", "tile_off2"):
