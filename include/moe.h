@@ -62,7 +62,11 @@ typedef enum {
   MOE_ROUTE_RENORMALIZE = 1,       /* top-k -> softmax over the k selected logits                 */
   MOE_ROUTE_DEEPSEEKV3 = 2,        /* sigmoid, +bias for selection, top-2 per group, top groups,
                                       top-k; weights = unbiased sigmoid / (sum + 1e-20) * rsf    */
+  MOE_ROUTE_LLAMA4 = 3,            /* top-k by logit ("Top1"), weights = sigmoid of each selected
+                                      logit, not renormalised                                     */
   MOE_ROUTE_RENORMALIZE_NAIVE = 4, /* softmax over E -> top-k -> divide by the selected sum       */
+  MOE_ROUTE_MINIMAX2 = 5,          /* sigmoid, +bias for selection, top-k over all E; weights =
+                                      unbiased sigmoid / their sum (bias optional, NULL = 0)     */
   MOE_ROUTE_SIGMOID_RENORM = 6     /* sigmoid -> top-k -> divide by the selected sum              */
 } moe_route_method;
 

@@ -37,7 +37,9 @@ int32_t route_reason(int64_t T, const moe_route_params& r) {
   switch (r.method) {
     case MOE_ROUTE_DEFAULT:
     case MOE_ROUTE_RENORMALIZE:
+    case MOE_ROUTE_LLAMA4:
     case MOE_ROUTE_RENORMALIZE_NAIVE:
+    case MOE_ROUTE_MINIMAX2:
     case MOE_ROUTE_SIGMOID_RENORM:
       return MOE_REASON_OK;
     case MOE_ROUTE_DEEPSEEKV3: {

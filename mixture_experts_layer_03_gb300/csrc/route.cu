@@ -6,6 +6,10 @@
 //   Renormalize      top-k, softmax over the k selected logits
 //   RenormalizeNaive softmax over all E, top-k, divide by the selected sum
 //   SigmoidRenorm    sigmoid, top-k, divide by the selected sum
+//   Llama4           "Top1 -> Sigmoid": top-k by logit, each weight the sigmoid of its own
+//                    logit, not renormalised
+//   MiniMax2         "Sigmoid -> RoutingBiasAdd -> TopK -> Renormalize(without bias)": the
+//                    DeepSeekV3 keys over all E (one group), weights = unbiased scores / sum
 //   DeepSeekV3       noaux_tc (same page, section "DeepSeek-V3 的 noaux_tc"): sigmoid
 //                    scores, + e_score_correction_bias for selection only, group score =
 //                    sum of the top-2 biased scores, keep topk_group groups, top-k among
@@ -13,7 +17,8 @@
 //
 // Selection keys are fp32 so ids are exact: the logit itself for the softmax and sigmoid
 // methods (both maps are increasing), and kappa = fl32(fl32(sigmoid_fp64(l)) + b) for
-// DeepSeekV3. Ties go to the lower expert index; slots are listed by descending key.
+// DeepSeekV3 and MiniMax2. Ties go to the lower expert index; slots are listed by
+// descending key.
 //
 // FP64 runs at 1/64 of the FP32 rate on this part, so it is used only where the result
 // depends on it:
@@ -110,7 +115,8 @@ __device__ __forceinline__ void warp_topk(const float (&key)[EPL], uint32_t live
 }
 
 // EPL = experts per lane (lane l holds experts l, l + 32, ...; E <= 32 * EPL).
-// kGrouped: the DeepSeekV3 grouped selection; otherwise the softmax/sigmoid methods.
+// kGrouped: selection on the biased sigmoid keys (DeepSeekV3 with groups, MiniMax2 with
+// one group); otherwise on the logits (the softmax/sigmoid methods and Llama4).
 template <int EPL, bool kGrouped>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __restrict__ bias,
@@ -174,7 +180,7 @@ route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __
       const int epg = E / n_group;
       float gscore = -INFINITY;
       int gidx = INT32_MAX;
-      if (lane < n_group) {
+      if (n_group > 1 && lane < n_group) {
         const int e0 = lane * epg;
         float a1 = -INFINITY, a2 = -INFINITY;
         for (int j = 0; j < epg; ++j) {
@@ -198,10 +204,11 @@ route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __
         gscore = __fadd_rn(x1, x2);
         gidx = lane;
       }
-      // Keep topk_group groups by repeated warp argmax (ties: lower group index).
-      uint32_t chosen = 0;
+      // Keep topk_group groups by repeated warp argmax (ties: lower group index). A single
+      // group is kept without scoring it.
+      uint32_t chosen = n_group > 1 ? 0u : 1u;
       bool gtaken = false;
-      for (int r = 0; r < topk_group; ++r) {
+      for (int r = 0; n_group > 1 && r < topk_group; ++r) {
         KeyIdx v = gtaken ? KeyIdx{-INFINITY, INT32_MAX} : KeyIdx{gscore, gidx};
         v = warp_best(v);
         if (v.idx == lane) gtaken = true;
@@ -286,7 +293,7 @@ route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __
     if (tt >= T) continue;
     const double lv = static_cast<double>(s_sel_l[w][j]);
     double e;
-    if (kGrouped || method == MOE_ROUTE_SIGMOID_RENORM)
+    if (kGrouped || method == MOE_ROUTE_SIGMOID_RENORM || method == MOE_ROUTE_LLAMA4)
       e = sigmoid_d(lv);
     else
       e = exp(lv - static_cast<double>(s_sel_l[w][0]));   // slot 0 holds the largest logit
@@ -302,6 +309,10 @@ route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __
     double wgt;
     if (method == MOE_ROUTE_DEFAULT)
       wgt = s_e[w][j] / s_z[w];
+    else if (method == MOE_ROUTE_LLAMA4)
+      wgt = s_e[w][j];
+    else if (method == MOE_ROUTE_MINIMAX2)
+      wgt = s_e[w][j] / s;
     else if (kGrouped)
       wgt = s_e[w][j] / (s + 1e-20) * static_cast<double>(rsf);
     else
@@ -315,11 +326,12 @@ template <int EPL, bool kGrouped>
 cudaError_t launch_route_t(const float* logits, int64_t T, const float* bias,
                            const moe_route_params& p, int32_t* ids, float* scales, cudaStream_t s) {
   const int64_t blocks = (T + kRouteWarps - 1) / kRouteWarps;
+  // Groups and the routed scaling factor belong to DeepSeekV3; MiniMax2 has one group.
+  const bool dsv3 = p.method == MOE_ROUTE_DEEPSEEKV3;
   return launch_pdl(route_kernel<EPL, kGrouped>, dim3(static_cast<unsigned>(blocks)),
                     dim3(kRouteWarps * 32), 0, s, logits, T, p.num_experts,
-                    kGrouped ? bias : nullptr, p.method, p.top_k, kGrouped ? p.n_group : 1,
-                    kGrouped ? p.topk_group : 1, kGrouped ? p.routed_scaling_factor : 1.0f, ids,
-                    scales);
+                    kGrouped ? bias : nullptr, p.method, p.top_k, dsv3 ? p.n_group : 1,
+                    dsv3 ? p.topk_group : 1, dsv3 ? p.routed_scaling_factor : 1.0f, ids, scales);
 }
 
 template <bool kGrouped>
@@ -338,9 +350,9 @@ moe_status launch_route(const float* logits, int64_t T, const float* bias,
                         const moe_route_params& p, int32_t* ids, float* scales,
                         cudaStream_t s) {
   if (T == 0) return MOE_OK;
-  const cudaError_t err = p.method == MOE_ROUTE_DEEPSEEKV3
-                              ? launch_route_e<true>(logits, T, bias, p, ids, scales, s)
-                              : launch_route_e<false>(logits, T, bias, p, ids, scales, s);
+  const bool keyed = p.method == MOE_ROUTE_DEEPSEEKV3 || p.method == MOE_ROUTE_MINIMAX2;
+  const cudaError_t err = keyed ? launch_route_e<true>(logits, T, bias, p, ids, scales, s)
+                                : launch_route_e<false>(logits, T, bias, p, ids, scales, s);
   if (err != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "route_kernel launch: %s", cudaGetErrorString(err));
   return MOE_OK;

@@ -3,10 +3,11 @@
 Importable by ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
 baseline / reference arm; never by the product path.
 """
-from .moe_oracle import (DEFAULT, RENORMALIZE, DEEPSEEKV3, RENORMALIZE_NAIVE, SIGMOID_RENORM,
-                         METHODS, topk_desc, softmax64, sigmoid64, deepseek_keys, group_select,
+from .moe_oracle import (DEFAULT, RENORMALIZE, DEEPSEEKV3, LLAMA4, RENORMALIZE_NAIVE, MINIMAX2,
+                         SIGMOID_RENORM, METHODS, topk_desc, softmax64, sigmoid64, deepseek_keys, group_select,
                          route, permute, swiglu, expert_ffn, forward, forward_permuted)
 
-__all__ = ["DEFAULT", "RENORMALIZE", "DEEPSEEKV3", "RENORMALIZE_NAIVE", "SIGMOID_RENORM",
+__all__ = ["DEFAULT", "RENORMALIZE", "DEEPSEEKV3", "LLAMA4", "RENORMALIZE_NAIVE", "MINIMAX2",
+           "SIGMOID_RENORM",
            "METHODS", "topk_desc", "softmax64", "sigmoid64", "deepseek_keys", "group_select",
            "route", "permute", "swiglu", "expert_ffn", "forward", "forward_permuted"]

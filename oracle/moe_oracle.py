@@ -21,6 +21,11 @@ with E_i a SwiGLU FFN. Readings taken where the pages are silent:
 * Selection for the softmax/sigmoid methods is top-k of the raw fp32 logit
   (softmax and sigmoid are strictly increasing, so the chosen set and its order
   are those of the scores); ties go to the lowest expert index.
+* Llama4 ("Top1 -> Sigmoid"): the top-k experts by logit (k = 1 in the model the
+  name refers to), each weighted by the sigmoid of its own logit, not renormalised.
+* MiniMaxM2 ("Sigmoid -> RoutingBiasAdd -> TopK -> Renormalize(without bias)"): the
+  DeepSeek-V3 key below without groups, weights = unbiased sigmoid / their sum (no
+  epsilon and no scaling factor: the pages name neither for this method).
 * DeepSeek-V3 selection key: kappa_e = fl32(fl32(sigmoid64(l_e)) + b_e), i.e.
   the sigmoid in float64 rounded once to fp32, then an IEEE fp32 add of the
   bias. Group score = fl32(top1 + top2 of kappa within the group). Ties: lowest
@@ -39,10 +44,12 @@ import numpy as np
 DEFAULT = 0
 RENORMALIZE = 1
 DEEPSEEKV3 = 2
+LLAMA4 = 3
 RENORMALIZE_NAIVE = 4
+MINIMAX2 = 5
 SIGMOID_RENORM = 6
 
-METHODS = (DEFAULT, RENORMALIZE, DEEPSEEKV3, RENORMALIZE_NAIVE, SIGMOID_RENORM)
+METHODS = (DEFAULT, RENORMALIZE, DEEPSEEKV3, LLAMA4, RENORMALIZE_NAIVE, MINIMAX2, SIGMOID_RENORM)
 
 
 # --------------------------------------------------------------------------- routing
@@ -107,7 +114,9 @@ def route(logits, method: int, top_k: int, bias=None, n_group: int = 1, topk_gro
       Default (0)           softmax -> top-k, weights = selected softmax probabilities
       Renormalize (1)       top-k -> softmax over the selected logits
       DeepSeekV3 (2)        sigmoid -> bias add -> top-2 per group -> top groups -> top-k
+      Llama4 (3)            top-k (Top1) -> sigmoid of each selected logit
       RenormalizeNaive (4)  softmax -> top-k -> divide by the selected sum
+      MiniMax2 (5)          sigmoid -> bias add -> top-k -> divide by the unbiased sum
       SigmoidRenorm (6)     sigmoid -> top-k -> divide by the selected sum
     VLLM, section "FusedTopKRouter": the same softmax/sigmoid -> top-k -> renormalize.
     """
@@ -115,6 +124,17 @@ def route(logits, method: int, top_k: int, bias=None, n_group: int = 1, topk_gro
     T, E = l32.shape
     sel = _selection_logits(l32)
     l64 = sel.astype(np.float64)
+    if method == LLAMA4:
+        ids = topk_desc(sel, top_k)
+        w = sigmoid64(np.take_along_axis(l64, ids, axis=1))
+        return ids.astype(np.int32), w
+    if method == MINIMAX2:
+        b = np.zeros(E, np.float32) if bias is None else np.asarray(bias, np.float32)
+        s64, kappa = deepseek_keys(l32, b)
+        ids = topk_desc(kappa, top_k)
+        ssel = np.take_along_axis(s64, ids, axis=1)
+        w = ssel / np.sum(ssel, axis=1, keepdims=True)
+        return ids.astype(np.int32), w
     if method in (DEFAULT, RENORMALIZE, RENORMALIZE_NAIVE, SIGMOID_RENORM):
         ids = topk_desc(sel, top_k)
         lsel = np.take_along_axis(l64, ids, axis=1)

@@ -96,7 +96,9 @@ def _route_params(moe, E, k, method, n_group=1, topk_group=1, rsf=1.0):
 
 @pytest.mark.parametrize("E,k,method,ng,tg,ok", [
     (8, 2, 4, 1, 1, True), (8, 9, 4, 1, 1, False), (8, 9, 0, 1, 1, False), (4, 5, 1, 1, 1, False),
-    (300, 2, 6, 1, 1, False), (8, 2, 3, 1, 1, False), (8, 2, 5, 1, 1, False),
+    (300, 2, 6, 1, 1, False), (8, 2, 3, 1, 1, True), (8, 2, 5, 1, 1, True),
+    (256, 8, 5, 1, 1, True), (300, 8, 5, 1, 1, False), (16, 9, 3, 1, 1, False),
+    (8, 2, 7, 1, 1, False), (8, 2, -1, 1, 1, False),   # no such method
     (256, 8, 2, 8, 4, True), (256, 8, 2, 7, 4, False), (256, 8, 2, 8, 9, False),
     (64, 8, 2, 1, 1, False),   # 64 experts in one group > 32 per group
     (8, 8, 2, 4, 2, False),    # k > topk_group * experts per group

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from workloads import (WORKLOADS, Workload, make_inputs, DEFAULT, RENORMALIZE, DEEPSEEKV3,
-                       RENORMALIZE_NAIVE, SIGMOID_RENORM)
+                       LLAMA4, RENORMALIZE_NAIVE, MINIMAX2, SIGMOID_RENORM)
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
@@ -69,6 +69,12 @@ ROUTE_CASES = [
     (64, 1, 1, SIGMOID_RENORM, 1, 1, 1.0, 1.0, False),        # one expert
     (64, 8, 8, DEFAULT, 1, 1, 1.0, 1.0, False),               # k = E
     (1, 256, 8, RENORMALIZE, 1, 1, 1.0, 1.0, False),          # one token
+    (257, 16, 1, LLAMA4, 1, 1, 1.0, 1.0, False),              # Top1 -> sigmoid
+    (100, 128, 1, LLAMA4, 1, 1, 1.0, 3.0, False),
+    (64, 16, 4, LLAMA4, 1, 1, 1.0, 1.0, True),                # k > 1, exact ties
+    (257, 256, 8, MINIMAX2, 1, 1, 1.0, 1.0, False),           # biased keys over all 256
+    (100, 64, 4, MINIMAX2, 1, 1, 1.0, 1.0, False),
+    (64, 16, 4, MINIMAX2, 1, 1, 1.0, 1.0, True),              # ties in the keys
 ]
 
 
@@ -80,7 +86,7 @@ def test_route_parity(moe, case):
         logits = torch.randint(-2, 3, (T, E), generator=g).float()
     else:
         logits = torch.randn(T, E, generator=g) * scale
-    bias = torch.randn(E, generator=g) * 0.1 if method == DEEPSEEKV3 else None
+    bias = torch.randn(E, generator=g) * 0.1 if method in (DEEPSEEKV3, MINIMAX2) else None
     ids, sc = moe.moe_route(logits.cuda(), method, k, bias=None if bias is None else bias.cuda(),
                             n_group=ng, topk_group=tg, routed_scaling_factor=rsf)
     ids_ref, sc_ref = oracle.route(logits.numpy(), method, k,
@@ -282,13 +288,14 @@ def test_cast_is_round_to_nearest_even(moe):
 # ------------------------------------------------------------------------ full-size workloads
 
 SAMPLE_TOKENS = {"tiny": 64, "mixtral_prefill": 16, "qwen3_decode": 16, "dsv3_layer": 4,
-                 "skewed": 16}
+                 "skewed": 16, "llama4_scout": 6, "minimax_m2": 6}
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["tiny", "mixtral_prefill", "qwen3_decode", "dsv3_layer", "skewed"])
+@pytest.mark.parametrize("name", ["tiny", "mixtral_prefill", "qwen3_decode", "dsv3_layer", "skewed",
+                                  "llama4_scout", "minimax_m2"])
 def test_workload_full_size(moe, name):
-    """The five workloads at full size, in the launch configuration the bench times
+    """The workloads at full size, in the launch configuration the bench times
     (moe_route then moe_forward on one stream). Routing, counts and permutation are
     checked on every token; y on sampled tokens (plus the edge tokens)."""
     w: Workload = WORKLOADS[name]

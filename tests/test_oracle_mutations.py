@@ -73,3 +73,34 @@ def test_unstable_permute_is_caught(monkeypatch):
     monkeypatch.setattr(om, "permute", bad_permute)
     monkeypatch.setattr(oracle, "permute", bad_permute)
     _fails(pins.test_permute_brute_force_and_identity)
+
+
+def test_renormalised_llama4_is_caught(monkeypatch, golden_dir):
+    real = om.route
+
+    def bad_route(logits, method, top_k, *a, **kw):
+        if method == om.LLAMA4:
+            method = om.SIGMOID_RENORM
+        return real(logits, method, top_k, *a, **kw)
+    monkeypatch.setattr(om, "route", bad_route)
+    monkeypatch.setattr(oracle, "route", bad_route)
+    _fails(pins.test_golden_llama4_and_minimax2, golden_dir)
+
+
+def test_minimax2_biased_weights_are_caught(monkeypatch, golden_dir):
+    real = om.deepseek_keys
+
+    def bad_keys(l, b):
+        s64, kappa = real(l, b)
+        return kappa.astype(np.float64), kappa
+    monkeypatch.setattr(om, "deepseek_keys", bad_keys)
+    _fails(pins.test_golden_llama4_and_minimax2, golden_dir)
+
+
+def test_minimax2_without_bias_is_caught(monkeypatch, golden_dir):
+    real = om.deepseek_keys
+
+    def bad_keys(l, b):
+        return real(l, np.zeros_like(b))
+    monkeypatch.setattr(om, "deepseek_keys", bad_keys)
+    _fails(pins.test_golden_llama4_and_minimax2, golden_dir)

@@ -13,7 +13,8 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle import DEFAULT, RENORMALIZE, DEEPSEEKV3, RENORMALIZE_NAIVE, SIGMOID_RENORM
+from oracle import (DEFAULT, RENORMALIZE, DEEPSEEKV3, LLAMA4, RENORMALIZE_NAIVE, MINIMAX2,
+                    SIGMOID_RENORM)
 
 
 def _ev(expr):
@@ -50,6 +51,22 @@ def test_golden_grouped_deepseek(golden_dir):
                            routed_scaling_factor=g["routed_scaling_factor"])
     assert ids[0].tolist() == g["expected_ids"]
     np.testing.assert_allclose(sc[0], [_ev(e) for e in g["expected_scales_expr"]], rtol=1e-6)
+
+
+def test_golden_llama4_and_minimax2(golden_dir):
+    g = _load(golden_dir, "route_llama4_minimax_hand.json")
+    for case in g["llama4"]:
+        logits = np.array([[_ev(e) for e in case["logits_expr"]]], np.float32)
+        ids, sc = oracle.route(logits, LLAMA4, case["top_k"])
+        assert ids[0].tolist() == case["expected_ids"]
+        np.testing.assert_allclose(sc[0], [_ev(e) for e in case["scales_expr"]], rtol=1e-6)
+    for case in g["minimax2"]:
+        p = np.array(case["probabilities"], np.float64)
+        logits = np.log(p / (1 - p)).astype(np.float32)[None, :]
+        ids, sc = oracle.route(logits, MINIMAX2, case["top_k"],
+                               bias=np.array(case["bias"], np.float32))
+        assert ids[0].tolist() == case["expected_ids"]
+        np.testing.assert_allclose(sc[0], [_ev(e) for e in case["scales_expr"]], rtol=1e-6)
 
 
 def test_golden_ffn_and_layer(golden_dir):
@@ -93,7 +110,8 @@ def _rank_select(keys, k):
     return out
 
 
-@pytest.mark.parametrize("method", [DEFAULT, RENORMALIZE, RENORMALIZE_NAIVE, SIGMOID_RENORM])
+@pytest.mark.parametrize("method", [DEFAULT, RENORMALIZE, LLAMA4, RENORMALIZE_NAIVE,
+                                    SIGMOID_RENORM])
 def test_topk_matches_rank_counting(method):
     rng = np.random.default_rng(1)
     for trial in range(60):
@@ -131,6 +149,7 @@ def test_weights_closed_forms():
             RENORMALIZE: _softmax_loop([l[e] for e in sel]),
             RENORMALIZE_NAIVE: [p[e] / sum(p[s] for s in sel) for e in sel],
             SIGMOID_RENORM: [s / sum(sig) for s in sig],
+            LLAMA4: sig,
         }
         for m, w in want.items():
             _, sc = oracle.route(logits[t:t + 1], m, k)
@@ -232,6 +251,33 @@ def test_bias_moves_selection_not_weights():
     for t in range(T):
         v = sig[t, ib[t]]
         np.testing.assert_allclose(sb[t], v / (v.sum() + 1e-20), rtol=1e-12)
+
+
+def test_minimax2_brute_force_and_single_group_deepseek():
+    rng = np.random.default_rng(7)
+    for trial in range(30):
+        E = int(rng.integers(2, 40))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        T = 6
+        if trial % 3 == 0:   # exact ties in the keys
+            logits = rng.integers(-2, 3, size=(T, E)).astype(np.float32)
+            b = np.zeros(E, np.float32)
+        else:
+            logits = rng.standard_normal((T, E)).astype(np.float32)
+            b = (0.3 * rng.standard_normal(E)).astype(np.float32)
+        ids, sc = oracle.route(logits, MINIMAX2, k, bias=b)
+        for t in range(T):
+            # keys by rank counting; weights by explicit loops over the unbiased sigmoid
+            kappa = [float(np.float32(np.float32(1 / (1 + math.exp(-float(l)))) + bb))
+                     for l, bb in zip(logits[t], b)]
+            sel = _rank_select(kappa, k)
+            assert ids[t].tolist() == sel
+            sig = [1 / (1 + math.exp(-float(logits[t][e]))) for e in sel]
+            np.testing.assert_allclose(sc[t], [v / sum(sig) for v in sig], rtol=1e-12)
+        i2, s2 = oracle.route(logits, DEEPSEEKV3, k, bias=b, n_group=1, topk_group=1,
+                              routed_scaling_factor=1.0)
+        assert np.array_equal(ids, i2)
+        np.testing.assert_allclose(sc, s2, rtol=1e-12)
 
 
 # ---------------------------------------------------------------- permute

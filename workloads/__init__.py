@@ -9,7 +9,7 @@ device the caller names, in this fixed order):
 
 1. ``logits`` [T, E] fp32 ~ N(0, 1) (plus a per-expert Zipf bias for the
    skewed workload, see ``zipf_logit_bias``);
-2. ``bias`` [E] fp32 ~ N(0, bias_std) (grouped DeepSeek-V3 routing only);
+2. ``bias`` [E] fp32 ~ N(0, bias_std) (the biased-key routings, DeepSeek-V3 and MiniMax2);
 3. ``x`` [T, H] ~ N(0, 1);
 4. ``w13`` [E, 2I, H], expert by expert, ~ N(0, std = H^-1/2);
 5. ``w2`` [E, H, I], expert by expert, ~ N(0, std = I^-1/2);
@@ -30,7 +30,9 @@ import torch
 DEFAULT = 0
 RENORMALIZE = 1
 DEEPSEEKV3 = 2
+LLAMA4 = 3
 RENORMALIZE_NAIVE = 4
+MINIMAX2 = 5
 SIGMOID_RENORM = 6
 
 
@@ -76,8 +78,16 @@ WORKLOADS = {
                            n_group=8, topk_group=4, rsf=2.5, shared_I=2048, bias_std=0.1),
     "skewed": Workload("skewed", T=8192, H=4096, I=1536, E=64, k=4, method=SIGMOID_RENORM,
                        zipf_s=1.2),
+    # Shapes of the two routing methods the TensorRT-LLM page names by model (Llama4:
+    # "Top1 -> Sigmoid"; MiniMaxM2: sigmoid + bias -> top-k -> renormalise without bias),
+    # taken from those models' published layer sizes.
+    "llama4_scout": Workload("llama4_scout", T=2048, H=5120, I=8192, E=16, k=1, method=LLAMA4,
+                             shared_I=8192),
+    "minimax_m2": Workload("minimax_m2", T=4096, H=3072, I=1536, E=256, k=8, method=MINIMAX2,
+                           bias_std=0.1),
 }
-ORDER = ["tiny", "mixtral_prefill", "qwen3_decode", "dsv3_layer", "skewed"]
+ORDER = ["tiny", "mixtral_prefill", "qwen3_decode", "dsv3_layer", "skewed", "llama4_scout",
+         "minimax_m2"]
 
 
 def zipf_logit_bias(E: int, s: float) -> torch.Tensor:
@@ -148,5 +158,5 @@ def min_bytes(w: Workload, n_active: int) -> float:
 
 
 __all__ = ["Workload", "WORKLOADS", "ORDER", "make_inputs", "small_case", "zipf_logit_bias",
-           "flops", "min_bytes", "DEFAULT", "RENORMALIZE", "DEEPSEEKV3", "RENORMALIZE_NAIVE",
-           "SIGMOID_RENORM"]
+           "flops", "min_bytes", "DEFAULT", "RENORMALIZE", "DEEPSEEKV3", "LLAMA4",
+           "RENORMALIZE_NAIVE", "MINIMAX2", "SIGMOID_RENORM"]
