@@ -25,11 +25,14 @@
 //  * weights: exp/sigmoid of the k selected logits and the divisions, in fp64, for all
 //    (token, slot) pairs of a block packed across threads; the Default normaliser over
 //    all E uses fp32 expf terms (relative error <= 2 ulp each) accumulated in fp64.
-//  * DeepSeekV3 keys: every kappa is first approximated in fp32 (|error| <= D, a bound
-//    with a wide margin); the exact fp64-derived kappa is then computed only for the
-//    experts that can still decide a group's top-2 sum or the final top-k. Every other
-//    expert is provably below the decision threshold, so the ids equal those from exact
-//    keys everywhere.
+//  * DeepSeekV3 / MiniMax2 keys: every kappa is first approximated in fp32 (|error| <= D,
+//    a bound with a wide margin). When every decision (the chosen groups, then each
+//    place of the top-k) is separated from the next candidate by more than twice its
+//    error bound, the approximate keys decide exactly as the exact ones would and no
+//    fp64 key is computed. Otherwise the token takes the exact path: the fp64-derived
+//    kappa only for the experts that can still decide a group's top-2 sum or the final
+//    top-k (every other expert is provably below the decision threshold). Either way the
+//    ids equal those from exact keys.
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
@@ -114,6 +117,39 @@ __device__ __forceinline__ void warp_topk(const float (&key)[EPL], uint32_t live
   if (kth_key) *kth_key = last;
 }
 
+// k + 1 rounds of warp argmax over approximate keys: the k winners in sel, and whether
+// every two consecutive keys among the k + 1 best (the (k+1)-th taken as -inf when there
+// is none) differ by more than 2 * D. Keys within D of the exact ones then select and
+// order exactly the same experts.
+template <int EPL>
+__device__ __forceinline__ bool warp_topk_separated(const float (&key)[EPL], uint32_t live, int k,
+                                                    int lane, float D, int (&sel)[kMaxTopK]) {
+  uint32_t taken = 0;
+  float prev = INFINITY;
+  bool sep = true;
+  for (int j = 0; j <= k; ++j) {
+    KeyIdx best{-INFINITY, INT32_MAX};
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (((live & ~taken) >> i) & 1u && beats(key[i], e, best.key, best.idx)) {
+        best.key = key[i];
+        best.idx = e;
+      }
+    }
+    best = warp_best(best);
+    const float cur = best.idx == INT32_MAX ? -INFINITY : best.key;
+    if (j > 0 && !(prev - cur > 2.0f * D)) sep = false;
+    if (j < k) {
+      if (best.idx == INT32_MAX) best.idx = 0;   // unreachable: callers pass >= k live keys
+      if ((best.idx & 31) == lane) taken |= 1u << (best.idx >> 5);
+      sel[j] = best.idx;
+    }
+    prev = cur;
+  }
+  return sep;
+}
+
 // EPL = experts per lane (lane l holds experts l, l + 32, ...; E <= 32 * EPL).
 // kGrouped: selection on the biased sigmoid keys (DeepSeekV3 with groups, MiniMax2 with
 // one group); otherwise on the logits (the softmax/sigmoid methods and Llama4).
@@ -174,80 +210,132 @@ route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __
       const float D = 1e-6f + 2.5e-7f * warp_max_f(amax);
       __syncwarp();
 
-      // Group scores: lane g sums the exact top-2 keys of its group. Only experts whose
-      // approximate key is within 2D of the approximate second-largest can be in the
-      // exact top-2; their keys are made exact first.
       const int epg = E / n_group;
-      float gscore = -INFINITY;
-      int gidx = INT32_MAX;
-      if (n_group > 1 && lane < n_group) {
-        const int e0 = lane * epg;
-        float a1 = -INFINITY, a2 = -INFINITY;
-        for (int j = 0; j < epg; ++j) {
-          const float v = s_key[warp][e0 + j];
-          if (v > a1) { a2 = a1; a1 = v; } else if (v > a2) { a2 = v; }
-        }
-        const float thr = a2 - 2.0f * D;
-        float x1 = -INFINITY, x2 = -INFINITY;
-        for (int j = 0; j < epg; ++j) {
-          const int e = e0 + j;
-          float v = s_key[warp][e];
-          if (v >= thr) {
-            if (!s_exact[warp][e]) {
-              v = exact_kappa(row[e], bias ? bias[e] : 0.0f);
-              s_key[warp][e] = v;
-              s_exact[warp][e] = 1;
-            }
-            if (v > x1) { x2 = x1; x1 = v; } else if (v > x2) { x2 = v; }
-          }
-        }
-        gscore = __fadd_rn(x1, x2);
-        gidx = lane;
-      }
-      // Keep topk_group groups by repeated warp argmax (ties: lower group index). A single
-      // group is kept without scoring it.
-      uint32_t chosen = n_group > 1 ? 0u : 1u;
-      bool gtaken = false;
-      for (int r = 0; n_group > 1 && r < topk_group; ++r) {
-        KeyIdx v = gtaken ? KeyIdx{-INFINITY, INT32_MAX} : KeyIdx{gscore, gidx};
-        v = warp_best(v);
-        if (v.idx == lane) gtaken = true;
-        chosen |= 1u << v.idx;
-      }
-      __syncwarp();
-
-      // Final top-k inside the chosen groups. Bounds per expert (exact: lb = ub = kappa);
-      // the k-th largest lower bound is a threshold no non-candidate can reach.
-      float lb[kMaxPerLane];
-      uint32_t live = 0;
-#pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
-        const int e = lane + 32 * i;
-        lb[i] = -INFINITY;
-        if (((present >> i) & 1u) && ((chosen >> (e / epg)) & 1u)) {
-          live |= 1u << i;
-          key[i] = s_key[warp][e];
-          lb[i] = s_exact[warp][e] ? key[i] : key[i] - D;
-        }
-      }
-      int tmp[kMaxTopK];
-      float kth_lb;
-      warp_topk(lb, live, k, lane, tmp, &kth_lb);
-      uint32_t cand = 0;
-#pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
-        const int e = lane + 32 * i;
-        if ((live >> i) & 1u) {
-          const bool ex = s_exact[warp][e];
-          const float ub = ex ? key[i] : key[i] + D;
-          if (ub >= kth_lb) {
-            cand |= 1u << i;
-            if (!ex) key[i] = exact_kappa(row[e], bias ? bias[e] : 0.0f);
-          }
-        }
-      }
       int sel[kMaxTopK];
-      warp_topk(key, cand, k, lane, sel, nullptr);
+
+      // Certified path: every decision taken on the approximate keys, accepted only when
+      // each one has a margin above the keys' error bound, so that the exact keys would
+      // decide the same way. (1) The chosen groups: the approximate group score (sum of
+      // the approximate top-2) is within 2D of the exact top-2 sum, plus one rounding of
+      // each sum, so Eg = 2D + 2.4e-7 |score| bounds its error; the last chosen group must
+      // beat the best left out by more than 2 Eg. (2) The top-k inside them: consecutive
+      // keys of the k + 1 best must differ by more than 2D.
+      bool certain = true;
+      uint32_t chosen = n_group > 1 ? 0u : 1u;
+      if (n_group > 1) {
+        float ga = -INFINITY;
+        int gi = INT32_MAX;
+        if (lane < n_group) {
+          const int e0 = lane * epg;
+          float a1 = -INFINITY, a2 = -INFINITY;
+          for (int j = 0; j < epg; ++j) {
+            const float v = s_key[warp][e0 + j];
+            if (v > a1) { a2 = a1; a1 = v; } else if (v > a2) { a2 = v; }
+          }
+          ga = __fadd_rn(a1, a2);
+          gi = lane;
+        }
+        const float Eg = 2.0f * D + 2.4e-7f * warp_max_f(lane < n_group ? fabsf(ga) : 0.0f);
+        bool gt = false;
+        float last = INFINITY, next = -INFINITY;
+        for (int r = 0; r <= topk_group && r < n_group; ++r) {
+          KeyIdx v = gt ? KeyIdx{-INFINITY, INT32_MAX} : KeyIdx{ga, gi};
+          v = warp_best(v);
+          if (r < topk_group) {
+            if (v.idx == lane) gt = true;
+            chosen |= 1u << v.idx;
+            last = v.key;
+          } else {
+            next = v.key;
+          }
+        }
+        if (topk_group < n_group && !(last - next > 2.0f * Eg)) certain = false;
+      }
+      if (certain) {
+        uint32_t live = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i) {
+          const int e = lane + 32 * i;
+          if (((present >> i) & 1u) && ((chosen >> (e / epg)) & 1u)) live |= 1u << i;
+        }
+        certain = warp_topk_separated(key, live, k, lane, D, sel);
+      }
+
+      if (!certain) {
+        // Exact path (rare): exact keys wherever a decision could depend on them.
+        // Group scores: lane g sums the exact top-2 keys of its group. Only experts whose
+        // approximate key is within 2D of the approximate second-largest can be in the
+        // exact top-2; their keys are made exact first.
+        float gscore = -INFINITY;
+        int gidx = INT32_MAX;
+        if (n_group > 1 && lane < n_group) {
+          const int e0 = lane * epg;
+          float a1 = -INFINITY, a2 = -INFINITY;
+          for (int j = 0; j < epg; ++j) {
+            const float v = s_key[warp][e0 + j];
+            if (v > a1) { a2 = a1; a1 = v; } else if (v > a2) { a2 = v; }
+          }
+          const float thr = a2 - 2.0f * D;
+          float x1 = -INFINITY, x2 = -INFINITY;
+          for (int j = 0; j < epg; ++j) {
+            const int e = e0 + j;
+            float v = s_key[warp][e];
+            if (v >= thr) {
+              if (!s_exact[warp][e]) {
+                v = exact_kappa(row[e], bias ? bias[e] : 0.0f);
+                s_key[warp][e] = v;
+                s_exact[warp][e] = 1;
+              }
+              if (v > x1) { x2 = x1; x1 = v; } else if (v > x2) { x2 = v; }
+            }
+          }
+          gscore = __fadd_rn(x1, x2);
+          gidx = lane;
+        }
+        // Keep topk_group groups by repeated warp argmax (ties: lower group index). A single
+        // group is kept without scoring it.
+        chosen = n_group > 1 ? 0u : 1u;
+        bool gtaken = false;
+        for (int r = 0; n_group > 1 && r < topk_group; ++r) {
+          KeyIdx v = gtaken ? KeyIdx{-INFINITY, INT32_MAX} : KeyIdx{gscore, gidx};
+          v = warp_best(v);
+          if (v.idx == lane) gtaken = true;
+          chosen |= 1u << v.idx;
+        }
+        __syncwarp();
+
+        // Final top-k inside the chosen groups. Bounds per expert (exact: lb = ub = kappa);
+        // the k-th largest lower bound is a threshold no non-candidate can reach.
+        float lb[kMaxPerLane];
+        uint32_t live = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i) {
+          const int e = lane + 32 * i;
+          lb[i] = -INFINITY;
+          if (((present >> i) & 1u) && ((chosen >> (e / epg)) & 1u)) {
+            live |= 1u << i;
+            key[i] = s_key[warp][e];
+            lb[i] = s_exact[warp][e] ? key[i] : key[i] - D;
+          }
+        }
+        int tmp[kMaxTopK];
+        float kth_lb;
+        warp_topk(lb, live, k, lane, tmp, &kth_lb);
+        uint32_t cand = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i) {
+          const int e = lane + 32 * i;
+          if ((live >> i) & 1u) {
+            const bool ex = s_exact[warp][e];
+            const float ub = ex ? key[i] : key[i] + D;
+            if (ub >= kth_lb) {
+              cand |= 1u << i;
+              if (!ex) key[i] = exact_kappa(row[e], bias ? bias[e] : 0.0f);
+            }
+          }
+        }
+        warp_topk(key, cand, k, lane, sel, nullptr);
+      }
       // Selected logits for the weights.
 #pragma unroll
       for (int j = 0; j < kMaxTopK; ++j) {

@@ -96,6 +96,23 @@ def test_route_parity(moe, case):
     np.testing.assert_allclose(sc.cpu().numpy(), sc_ref, rtol=1e-6, atol=0)
 
 
+@pytest.mark.parametrize("method,E,ng,tg", [(DEEPSEEKV3, 256, 8, 4), (MINIMAX2, 128, 1, 1)])
+def test_route_near_ties_in_biased_keys(moe, method, E, ng, tg):
+    """Keys that differ by about one fp32 ulp, where the fp32 approximation of the keys
+    cannot decide the order: the ids must still match the exact-key oracle."""
+    g = torch.Generator().manual_seed(21)
+    T = 256
+    logits = torch.randn(T, E, generator=g)
+    # every other expert gets the next fp32 logit above its neighbour's
+    logits[:, 1::2] = torch.nextafter(logits[:, 0::2], torch.full_like(logits[:, 0::2], 10.0))
+    bias = torch.zeros(E)
+    ids, sc = moe.moe_route(logits.cuda(), method, 8, bias=bias.cuda(), n_group=ng, topk_group=tg)
+    ids_ref, sc_ref = oracle.route(logits.numpy(), method, 8, bias=bias.numpy(), n_group=ng,
+                                   topk_group=tg)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(sc.cpu().numpy(), sc_ref, rtol=1e-6, atol=0)
+
+
 def test_route_nonfinite_logits_never_beat_finite(moe):
     logits = torch.randn(32, 16)
     logits[:, 3] = float("nan")
