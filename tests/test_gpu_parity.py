@@ -145,10 +145,10 @@ def test_permute_parity(moe, T, E, k):
     assert np.array_equal(ws.region("perm_inv", P, torch.int32).cpu().numpy(), perm_inv)
     xp = ws.region("x_perm", P * H, torch.bfloat16).view(P, H).cpu()
     assert torch.equal(xp, x[torch.from_numpy(perm_src).long() // k])
-    # work lists (one channel tile each here: I = 64, H = 128). When T * k >= 128 * E the
+    # work lists (one channel tile each here: I = 64, H = 128). When T * k >= 256 * E the
     # CTA-pair kernel takes every group: floor(m / 256) + (m % 256 > 0) units each.
     # Otherwise every group has ceil(m / 128) tiles in the single-SM list.
-    big = (counts >= 1) & (T * k >= 128 * E)
+    big = (counts >= 1) & (T * k >= 256 * E)
     pair_units = np.where(big, counts // 256 + (counts % 256 > 0), 0)
     single_tiles = np.where(big, 0, counts // 128 + (counts % 128 > 0))
     for name in ("tile_off1", "tile_off2"):
@@ -210,8 +210,8 @@ SMALL_CASES = [
     (300, 256, 192, 8, 2, 0, "route"),         # weight-major tiles, ragged FC1 channel tile
     (700, 384, 320, 4, 2, 0, "route"),         # token-major + remainder tiles, ragged FC2 tile
     (1000, 256, 256, 8, 1, 0, "one_expert"),   # one expert holds every row (7 full tiles + 104)
-    (1100, 256, 256, 8, 1, 0, "one_expert"),   # CTA pairs: 4 units + 76 rows (weight-major)
-    (1200, 384, 320, 8, 1, 0, "one_expert"),   # CTA pairs: 4 units + 176 rows (masked pair)
+    (1100, 256, 256, 4, 1, 0, "one_expert"),   # CTA pairs: 4 units + 76 rows (weight-major)
+    (1200, 384, 320, 4, 1, 0, "one_expert"),   # CTA pairs: 4 units + 176 rows (masked pair)
     (2200, 256, 192, 4, 2, 256, "route"),      # CTA pairs for routed and shared groups
     (513, 128, 128, 8, 8, 0, "route"),         # k = E: every expert every token
     (200, 192, 128, 16, 4, 128, "random_dup"), # repeated ids in a row, shared expert
