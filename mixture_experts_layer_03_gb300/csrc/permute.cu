@@ -255,6 +255,13 @@ gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ p
     uint4* d = reinterpret_cast<uint4*>(x_perm + r * H);
     // Four independent 16-byte loads in flight per lane before their stores.
     int v = lane;
+    for (; v + 224 < nvec; v += 256) {
+      uint4 a[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) a[q] = __ldg(s + v + 32 * q);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) __stcs(d + v + 32 * q, a[q]);
+    }
     for (; v + 96 < nvec; v += 128) {
       const uint4 a0 = __ldg(s + v), a1 = __ldg(s + v + 32), a2 = __ldg(s + v + 64),
                   a3 = __ldg(s + v + 96);
