@@ -209,6 +209,21 @@ moe_status moe_forward_static(const moe_problem* p, const void* x, const int32_t
                               const float* scales, const void* w13, const void* w2,
                               const void* w13_s, const void* w2_s, void* y, void* stream);
 
+/* moe_forward restricted to the experts [e_lo, e_hi) of this call: the expert-parallel
+ * seam of the TensorRT-LLM MoE page, section on supports_finalize_before_combine ("finalize
+ * before combine": the top-k weighted sum taken on a rank's own rows, slots of other
+ * ranks' experts contributing exactly 0, so that the combine is an unweighted row sum).
+ *   y[t] = sum over j with ids[t,j] in [e_lo, e_hi) of scales[t,j] * E_{ids[t,j]}(x[t])
+ *          (+ shared(x[t]) when p->shared_I > 0)
+ * The y of calls over a partition of [0, E) (the shared expert in exactly one of them) add
+ * up to moe_forward's y. w13 / w2 hold the local experts only: [e_hi - e_lo, 2I, H] and
+ * [e_hi - e_lo, H, I], expert g at plane g - e_lo. Requires 0 <= e_lo < e_hi <= E; ids in
+ * [0, E) outside the range are not errors. moe_forward is this call with [0, E). */
+moe_status moe_forward_partial(const moe_problem* p, int32_t e_lo, int32_t e_hi, const void* x,
+                               const int32_t* ids, const float* scales, const void* w13,
+                               const void* w2, const void* w13_s, const void* w2_s, void* y,
+                               void* workspace, size_t ws_bytes, void* stream);
+
 /* Step entry points (the kernels moe_forward runs, one at a time). Each takes the
  * same workspace; later steps read what earlier ones wrote into it. */
 

@@ -69,6 +69,9 @@ _SIGS = {
                                    ctypes.c_size_t, _P]),
     "moe_forward_static": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, _P, _P, _P, _P,
                                           _P, _P]),
+    "moe_forward_partial": (ctypes.c_int, [ctypes.POINTER(MoeProblem), ctypes.c_int32,
+                                           ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                           ctypes.c_size_t, _P]),
     "moe_permute": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_fc1": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_fc2": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
@@ -218,6 +221,33 @@ def moe_forward(x, ids, scales, w13, w2, w13_s=None, w2_s=None, y=None,
     _check(_lib.moe_forward(ctypes.byref(p), _ptr(x), _ptr(ids), _ptr(scales), _ptr(w13), _ptr(w2),
                             _ptr(w13_s), _ptr(w2_s), _ptr(y), workspace.ptr, workspace.nbytes,
                             _stream(stream)), "moe_forward")
+    return y
+
+
+def moe_forward_partial(x, ids, scales, w13_local, w2_local, e_lo: int, e_hi: int, num_experts: int,
+                        w13_s=None, w2_s=None, y=None, workspace: Optional[Workspace] = None,
+                        stream=None):
+    """moe_forward over the experts [e_lo, e_hi) of num_experts only (the expert-parallel
+    seam): slots routed elsewhere contribute 0. w13_local / w2_local hold those experts'
+    weights, [e_hi - e_lo, 2I, H] / [e_hi - e_lo, H, I]. Returns y bf16 [T, H]."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(ids, "ids", torch.int32)
+    _cuda(scales, "scales", torch.float32)
+    _cuda(w13_local, "w13_local", torch.bfloat16)
+    _cuda(w2_local, "w2_local", torch.bfloat16)
+    T, H = x.shape
+    k = ids.shape[1]
+    I = w2_local.shape[2]
+    shared_I = 0 if w13_s is None else w13_s.shape[0] // 2
+    p = make_problem(T, H, I, num_experts, k, shared_I)
+    if workspace is None:
+        workspace = alloc_workspace(p, x.device)
+    if y is None:
+        y = torch.empty_like(x)
+    _check(_lib.moe_forward_partial(ctypes.byref(p), int(e_lo), int(e_hi), _ptr(x), _ptr(ids),
+                                    _ptr(scales), _ptr(w13_local), _ptr(w2_local), _ptr(w13_s),
+                                    _ptr(w2_s), _ptr(y), workspace.ptr, workspace.nbytes,
+                                    _stream(stream)), "moe_forward_partial")
     return y
 
 

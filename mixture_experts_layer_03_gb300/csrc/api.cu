@@ -203,7 +203,8 @@ moe_status moe_permute(const moe_problem* p, const void* x, const int32_t* ids, 
   if (st != MOE_OK || p->T == 0) return st;
   if (!x || !ids || !aligned16(x) || !aligned16(ids))
     return set_error(MOE_ERR_INVALID_ARG, "x/ids NULL or not 16-byte aligned");
-  return launch_permute(*p, L, x, ids, static_cast<char*>(workspace), static_cast<cudaStream_t>(stream));
+  return launch_permute(*p, L, x, ids, 0, p->E, static_cast<char*>(workspace),
+                        static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_fc1(const moe_problem* p, const void* w13, const void* w13_s, void* workspace,
@@ -213,7 +214,8 @@ moe_status moe_fc1(const moe_problem* p, const void* w13, const void* w13_s, voi
   if (st != MOE_OK || p->T == 0) return st;
   if (!w13 || !aligned16(w13) || !shared_args_ok(p, w13_s, w13_s))
     return set_error(MOE_ERR_INVALID_ARG, "w13/w13_s NULL or not 16-byte aligned");
-  return launch_fc1(*p, L, w13, w13_s, static_cast<char*>(workspace), static_cast<cudaStream_t>(stream));
+  return launch_fc1(*p, L, w13, w13_s, 0, p->E, static_cast<char*>(workspace),
+                    static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_fc2(const moe_problem* p, const void* w2, const void* w2_s, void* workspace,
@@ -223,7 +225,8 @@ moe_status moe_fc2(const moe_problem* p, const void* w2, const void* w2_s, void*
   if (st != MOE_OK || p->T == 0) return st;
   if (!w2 || !aligned16(w2) || !shared_args_ok(p, w2_s, w2_s))
     return set_error(MOE_ERR_INVALID_ARG, "w2/w2_s NULL or not 16-byte aligned");
-  return launch_fc2(*p, L, w2, w2_s, static_cast<char*>(workspace), static_cast<cudaStream_t>(stream));
+  return launch_fc2(*p, L, w2, w2_s, 0, p->E, static_cast<char*>(workspace),
+                    static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_finalize(const moe_problem* p, const float* scales, void* y, void* workspace,
@@ -237,12 +240,15 @@ moe_status moe_finalize(const moe_problem* p, const float* scales, void* y, void
                          static_cast<cudaStream_t>(stream));
 }
 
-moe_status moe_forward(const moe_problem* p, const void* x, const int32_t* ids, const float* scales,
-                       const void* w13, const void* w2, const void* w13_s, const void* w2_s, void* y,
-                       void* workspace, size_t ws_bytes, void* stream) {
+moe_status moe_forward_partial(const moe_problem* p, int32_t e_lo, int32_t e_hi, const void* x,
+                               const int32_t* ids, const float* scales, const void* w13,
+                               const void* w2, const void* w13_s, const void* w2_s, void* y,
+                               void* workspace, size_t ws_bytes, void* stream) {
   moe_ws_layout L;
   moe_status st = check_forward_common(p, workspace, ws_bytes, &L);
   if (st != MOE_OK || p->T == 0) return st;
+  if (e_lo < 0 || e_hi > p->E || e_lo >= e_hi)
+    return set_error(MOE_ERR_INVALID_ARG, "expert range [%d, %d) not inside [0, %d)", e_lo, e_hi, p->E);
   if (!x || !ids || !scales || !w13 || !w2 || !y)
     return set_error(MOE_ERR_INVALID_ARG, "NULL tensor argument");
   if (!aligned16(x) || !aligned16(ids) || !aligned16(scales) || !aligned16(w13) || !aligned16(w2) ||
@@ -252,10 +258,17 @@ moe_status moe_forward(const moe_problem* p, const void* x, const int32_t* ids, 
     return set_error(MOE_ERR_INVALID_ARG, "shared expert weights NULL or not 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  if ((st = launch_permute(*p, L, x, ids, ws, s)) != MOE_OK) return st;
-  if ((st = launch_fc1(*p, L, w13, w13_s, ws, s)) != MOE_OK) return st;
-  if ((st = launch_fc2(*p, L, w2, w2_s, ws, s)) != MOE_OK) return st;
+  if ((st = launch_permute(*p, L, x, ids, e_lo, e_hi, ws, s)) != MOE_OK) return st;
+  if ((st = launch_fc1(*p, L, w13, w13_s, e_lo, e_hi, ws, s)) != MOE_OK) return st;
+  if ((st = launch_fc2(*p, L, w2, w2_s, e_lo, e_hi, ws, s)) != MOE_OK) return st;
   return launch_finalize(*p, L, scales, y, ws, s);
+}
+
+moe_status moe_forward(const moe_problem* p, const void* x, const int32_t* ids, const float* scales,
+                       const void* w13, const void* w2, const void* w13_s, const void* w2_s, void* y,
+                       void* workspace, size_t ws_bytes, void* stream) {
+  return moe_forward_partial(p, 0, p ? p->E : 0, x, ids, scales, w13, w2, w13_s, w2_s, y,
+                             workspace, ws_bytes, stream);
 }
 
 }  // extern "C"
@@ -319,9 +332,9 @@ moe_status moe_forward_static(const moe_problem* p, const void* x, const int32_t
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The permute step clears the status word and the GEMM tile counters in the scratch.
-  if ((st = launch_permute(*p, L, x, ids, ws, s)) != MOE_OK) return st;
-  if ((st = launch_fc1(*p, L, w13, w13_s, ws, s)) != MOE_OK) return st;
-  if ((st = launch_fc2(*p, L, w2, w2_s, ws, s)) != MOE_OK) return st;
+  if ((st = launch_permute(*p, L, x, ids, 0, p->E, ws, s)) != MOE_OK) return st;
+  if ((st = launch_fc1(*p, L, w13, w13_s, 0, p->E, ws, s)) != MOE_OK) return st;
+  if ((st = launch_fc2(*p, L, w2, w2_s, 0, p->E, ws, s)) != MOE_OK) return st;
   return launch_finalize(*p, L, scales, y, ws, s);
 }
 

@@ -78,6 +78,7 @@ struct GemmArgs {
   const int32_t* tile_off;  // [G+1] offsets into this kernel's work list
   int32_t G;
   int32_t E;                // routed groups; group E (if G > E) uses the shared maps
+  int32_t plane_off;        // routed expert g reads weight plane g - plane_off
   int32_t K_routed, K_shared;
   int32_t N_routed, N_shared;   // FC1: I / shared_I (channels); FC2: H
   __nv_bfloat16* out;
@@ -433,7 +434,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
         const Unit t = decode_single(tile, s_off, s_cnt, s_start, a, kFc1);
         const bool shared = t.g >= a.E;
         const CUtensorMap* mw = shared ? &map_ws : &map_w;
-        const int ecoord = shared ? 0 : t.g;
+        const int ecoord = shared ? 0 : t.g - a.plane_off;
         const int wr0 = t.n0;
         const int wr1 = kFc1 ? (t.N + t.n0) : (t.n0 + 128);
         const uint32_t bytes =
@@ -790,7 +791,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
         const bool shared = t.g >= a.E;
         const CUtensorMap* mw128 = shared ? &map_ws128 : &map_w128;
         const CUtensorMap* mw64 = shared ? &map_ws64 : &map_w64;
-        const int ecoord = shared ? 0 : t.g;
+        const int ecoord = shared ? 0 : t.g - a.plane_off;
         const int r = static_cast<int>(rank);
         // This CTA's token rows and its share of the weight rows.
         const int half = t.ntok >> 1;
@@ -1026,7 +1027,7 @@ moe_status prepare_kernels(int* max_clusters) {
 
 template <bool kFc1>
 moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void* w,
-                       const void* w_s, char* ws, cudaStream_t s) {
+                       const void* w_s, int e_lo, int e_hi, char* ws, cudaStream_t s) {
   int max_clusters = 1;
   moe_status st = prepare_kernels<kFc1>(&max_clusters);
   if (st != MOE_OK) return st;
@@ -1043,11 +1044,13 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
   const uint64_t wk = kFc1 ? static_cast<uint64_t>(p.H) : static_cast<uint64_t>(p.I);
   const uint64_t sr = kFc1 ? 2ull * p.shared_I : static_cast<uint64_t>(p.H);
   const uint64_t sk = kFc1 ? static_cast<uint64_t>(p.H) : static_cast<uint64_t>(p.shared_I);
-  ok = ok && encode_map3(&mw128, w, p.E, wr, wk, 128) && encode_map3(&mw64, w, p.E, wr, wk, 64);
+  // Routed weights hold the experts [e_lo, e_hi) of this call only.
+  const uint64_t planes = static_cast<uint64_t>(e_hi - e_lo);
+  ok = ok && encode_map3(&mw128, w, planes, wr, wk, 128) && encode_map3(&mw64, w, planes, wr, wk, 64);
   if (has_shared)
     ok = ok && encode_map3(&mws128, w_s, 1, sr, sk, 128) && encode_map3(&mws64, w_s, 1, sr, sk, 64);
   else
-    ok = ok && encode_map3(&mws128, w, p.E, wr, wk, 128) && encode_map3(&mws64, w, p.E, wr, wk, 64);
+    ok = ok && encode_map3(&mws128, w, planes, wr, wk, 128) && encode_map3(&mws64, w, planes, wr, wk, 64);
   if (!ok) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
   GemmArgs a;
@@ -1055,6 +1058,7 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
   a.starts = reinterpret_cast<const int32_t*>(ws + L.starts);
   a.G = L.groups;
   a.E = p.E;
+  a.plane_off = e_lo;
   if (kFc1) {
     a.K_routed = p.H;
     a.K_shared = p.H;
@@ -1112,13 +1116,13 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
 }  // namespace
 
 moe_status launch_fc1(const moe_problem& p, const moe_ws_layout& L, const void* w13,
-                      const void* w13_s, char* ws, cudaStream_t s) {
-  return launch_gemm<true>(p, L, w13, w13_s, ws, s);
+                      const void* w13_s, int e_lo, int e_hi, char* ws, cudaStream_t s) {
+  return launch_gemm<true>(p, L, w13, w13_s, e_lo, e_hi, ws, s);
 }
 
 moe_status launch_fc2(const moe_problem& p, const moe_ws_layout& L, const void* w2,
-                      const void* w2_s, char* ws, cudaStream_t s) {
-  return launch_gemm<false>(p, L, w2, w2_s, ws, s);
+                      const void* w2_s, int e_lo, int e_hi, char* ws, cudaStream_t s) {
+  return launch_gemm<false>(p, L, w2, w2_s, e_lo, e_hi, ws, s);
 }
 
 }  // namespace moe

@@ -44,14 +44,16 @@ moe_status launch_route(const float* logits, int64_t T, const float* bias,
                         const moe_route_params& p, int32_t* ids, float* scales,
                         cudaStream_t s);
 
+// Experts [e_lo, e_hi) are this call's (all of them: 0, E). Routed weights hold those
+// experts only (plane g - e_lo for expert g).
 moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const void* x,
-                          const int32_t* ids, char* ws, cudaStream_t s);
+                          const int32_t* ids, int e_lo, int e_hi, char* ws, cudaStream_t s);
 
 moe_status launch_fc1(const moe_problem& p, const moe_ws_layout& L, const void* w13,
-                      const void* w13_s, char* ws, cudaStream_t s);
+                      const void* w13_s, int e_lo, int e_hi, char* ws, cudaStream_t s);
 
 moe_status launch_fc2(const moe_problem& p, const moe_ws_layout& L, const void* w2,
-                      const void* w2_s, char* ws, cudaStream_t s);
+                      const void* w2_s, int e_lo, int e_hi, char* ws, cudaStream_t s);
 
 moe_status launch_finalize(const moe_problem& p, const moe_ws_layout& L, const float* scales,
                            void* y, const char* ws, cudaStream_t s);

@@ -25,8 +25,8 @@ namespace {
 constexpr int kPermWarps = kPermThreads / 32;
 
 __global__ void __launch_bounds__(kPermThreads)
-hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int32_t* __restrict__ block_hist,
-            int32_t* __restrict__ status) {
+hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int e_lo, int e_hi,
+            int32_t* __restrict__ block_hist, int32_t* __restrict__ status) {
   __shared__ int32_t h[256];
   pdl_trigger();
   for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
@@ -38,7 +38,7 @@ hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int32_t* __restri
   const int64_t f1 = (P < f0 + kPermChunk ? P : f0 + kPermChunk);
   for (int64_t f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
     const int e = ids[f];
-    if (e >= 0 && e < E) atomicAdd(&h[e], 1);
+    if (e >= e_lo && e < e_hi) atomicAdd(&h[e], 1);   // local experts only
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) block_hist[blockIdx.x * E + e] = h[e];
@@ -80,6 +80,7 @@ struct PlanArgs {
   int64_t P;
   int T;
   int E;
+  int e_lo, e_hi;      // the experts of this call; slots of others contribute nothing
   int k;
   int nb;
   int has_shared;
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
     __syncthreads();
     for (int64_t f = tid; f < a.P; f += blockDim.x) {
       const int e = a.ids[f];
-      if (e >= 0 && e < E) atomicAdd(&s_run[e], 1);
+      if (e >= a.e_lo && e < a.e_hi) atomicAdd(&s_run[e], 1);
     }
     __syncthreads();
     if (tid < E) tot = s_run[tid];
@@ -206,6 +207,9 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
         a.perm_inv[f] = -1;
         atomicOr(a.status, MOE_DEVICE_FLAG_BAD_ID);
         e = -1;
+      } else if (e < a.e_lo || e >= a.e_hi) {
+        a.perm_inv[f] = -1;   // another call's expert: this slot adds exactly 0 here
+        e = -1;
       }
     }
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
@@ -277,7 +281,7 @@ gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ p
 }  // namespace
 
 moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const void* x,
-                          const int32_t* ids, char* ws, cudaStream_t s) {
+                          const int32_t* ids, int e_lo, int e_hi, char* ws, cudaStream_t s) {
   const int64_t P = p.T * p.k;
   const int nb = L.n_chunks;
   PlanArgs a;
@@ -285,6 +289,8 @@ moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const vo
   a.P = P;
   a.T = static_cast<int>(p.T);
   a.E = p.E;
+  a.e_lo = e_lo;
+  a.e_hi = e_hi;
   a.k = p.k;
   a.nb = nb;
   a.has_shared = p.shared_I > 0;
@@ -306,7 +312,7 @@ moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const vo
   if (nb == 1) {
     err = launch_pdl(plan_kernel<true>, dim3(1), dim3(kPermThreads), 0, s, a);
   } else {
-    err = launch_pdl(hist_kernel, dim3(nb), dim3(kPermThreads), 0, s, ids, P, p.E,
+    err = launch_pdl(hist_kernel, dim3(nb), dim3(kPermThreads), 0, s, ids, P, p.E, e_lo, e_hi,
                      reinterpret_cast<int32_t*>(ws + L.block_hist), a.status);
     if (err == cudaSuccess) err = launch_pdl(plan_kernel<false>, dim3(nb), dim3(kPermThreads), 0, s, a);
   }

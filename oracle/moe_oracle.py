@@ -230,6 +230,31 @@ def forward(x, ids, scales, w13, w2, w13_s=None, w2_s=None) -> np.ndarray:
     return y
 
 
+def forward_partial(x, ids, scales, w13_local, w2_local, e_lo: int, e_hi: int, w13_s=None,
+                    w2_s=None) -> np.ndarray:
+    """The layer restricted to the experts [e_lo, e_hi): the slots whose expert lies
+    there, weighted by their scales (+ the shared expert when given).
+
+    TRT, section on supports_finalize_before_combine: with the top-k weighted sum taken
+    on each rank's own rows, the slots of other ranks' experts contribute exactly 0, so
+    the combine is an unweighted row sum. ``w13_local[e - e_lo]`` holds expert e.
+    """
+    X = np.asarray(x, dtype=np.float64)
+    ids = np.asarray(ids)
+    scales = np.asarray(scales, dtype=np.float64)
+    T, H = X.shape
+    y = np.zeros((T, H), dtype=np.float64)
+    for e in range(e_lo, e_hi):
+        rows, slots = np.nonzero(ids == e)
+        if rows.size == 0:
+            continue
+        o = expert_ffn(X[rows], w13_local[e - e_lo], w2_local[e - e_lo])
+        np.add.at(y, rows, scales[rows, slots][:, None] * o)
+    if w13_s is not None:
+        y += expert_ffn(X, w13_s, w2_s)
+    return y
+
+
 def forward_permuted(x, ids, scales, w13, w2, w13_s=None, w2_s=None):
     """The same result computed in the five-step order of the pages.
 

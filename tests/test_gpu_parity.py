@@ -253,6 +253,36 @@ def test_forward_steps_parity(moe, case):
     assert torch.equal(y2, y)
 
 
+@pytest.mark.parametrize("T,H,I,E,k,sI,cuts", [
+    (300, 256, 192, 8, 2, 128, [(0, 3), (3, 8)]),          # single-SM GEMM path
+    (2200, 256, 192, 4, 2, 256, [(0, 1), (1, 2), (2, 4)]),  # CTA-pair GEMM path
+    (200, 128, 128, 16, 4, 0, [(0, 5), (5, 6), (6, 16)]),   # a one-expert range
+])
+def test_forward_partial_over_a_partition(moe, T, H, I, E, k, sI, cuts):
+    """The expert-parallel seam: each range's y against the oracle's restricted sum, and
+    the ranges' y (shared expert in the first) adding up to moe_forward's y."""
+    c = _random_case(T, H, I, E, k, sI, seed=T + E)
+    dev = {n: (None if v is None else (torch.from_numpy(v) if isinstance(v, np.ndarray) else v).cuda())
+           for n, v in c.items()}
+    y_full = moe.moe_forward(dev["x"], dev["ids"], dev["sc"], dev["w13"], dev["w2"], dev["w13s"],
+                             dev["w2s"])
+    x64 = _np64(c["x"])
+    total = torch.zeros(T, H, dtype=torch.float32, device="cuda")
+    for n, (lo, hi) in enumerate(cuts):
+        w13s, w2s = (dev["w13s"], dev["w2s"]) if n == 0 else (None, None)
+        y = moe.moe_forward_partial(dev["x"], dev["ids"], dev["sc"], dev["w13"][lo:hi].contiguous(),
+                                    dev["w2"][lo:hi].contiguous(), lo, hi, E, w13s, w2s)
+        torch.cuda.synchronize()
+        ref = oracle.forward_partial(x64, c["ids"], c["sc"], _np64(c["w13"][lo:hi]),
+                                     _np64(c["w2"][lo:hi]), lo, hi,
+                                     None if w13s is None else _np64(c["w13s"]),
+                                     None if w2s is None else _np64(c["w2s"]))
+        _check_close(y.cpu().double().numpy(), ref, Y_TOL, f"partial [{lo}, {hi})")
+        total += y.float()
+    _check_close(total.cpu().double().numpy(), y_full.cpu().double().numpy(), Y_TOL,
+                 "sum of the partials vs moe_forward")
+
+
 def test_forward_is_deterministic(moe):
     c = _random_case(2000, 256, 256, 16, 4, 0, seed=3)
     _, ws, y1, dev = _run_forward_steps(moe, c)

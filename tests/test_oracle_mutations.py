@@ -104,3 +104,19 @@ def test_minimax2_without_bias_is_caught(monkeypatch, golden_dir):
         return real(l, np.zeros_like(b))
     monkeypatch.setattr(om, "deepseek_keys", bad_keys)
     _fails(pins.test_golden_llama4_and_minimax2, golden_dir)
+
+
+def test_partial_ignoring_scales_is_caught(monkeypatch):
+    def bad_partial(x, ids, scales, w13_local, w2_local, e_lo, e_hi, w13_s=None, w2_s=None):
+        X = np.asarray(x, dtype=np.float64)
+        y = np.zeros_like(X)
+        for e in range(e_lo, e_hi):
+            rows, slots = np.nonzero(np.asarray(ids) == e)
+            if rows.size:
+                np.add.at(y, rows, om.expert_ffn(X[rows], w13_local[e - e_lo], w2_local[e - e_lo]))
+        if w13_s is not None:
+            y += om.expert_ffn(X, w13_s, w2_s)
+        return y
+    monkeypatch.setattr(om, "forward_partial", bad_partial)
+    monkeypatch.setattr(oracle, "forward_partial", bad_partial)
+    _fails(pins.test_partial_forward_partition_and_zeroed_scales)

@@ -379,6 +379,31 @@ def test_layer_against_loops_linearity_and_equivariance():
         np.testing.assert_allclose(yd[t], want, rtol=1e-10)
 
 
+def test_partial_forward_partition_and_zeroed_scales():
+    """The expert-range forward: partials over a partition of [0, E) (the shared expert in
+    one of them) add up to the layer; each partial equals the layer with the scales of
+    the other experts' slots set to 0 (a different computation: all experts run)."""
+    rng = np.random.default_rng(9)
+    T, H, I, E, k, Is = 12, 6, 5, 6, 3, 4
+    x = rng.standard_normal((T, H))
+    w13 = rng.standard_normal((E, 2 * I, H)) * 0.5
+    w2 = rng.standard_normal((E, H, I)) * 0.5
+    w13s = rng.standard_normal((2 * Is, H)) * 0.5
+    w2s = rng.standard_normal((H, Is)) * 0.5
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    scales = rng.random((T, k))
+    full = oracle.forward(x, ids, scales, w13, w2, w13s, w2s)
+    cuts = [(0, 2), (2, 5), (5, 6)]
+    parts = []
+    for n, (lo, hi) in enumerate(cuts):
+        sh = (w13s, w2s) if n == 0 else (None, None)
+        parts.append(oracle.forward_partial(x, ids, scales, w13[lo:hi], w2[lo:hi], lo, hi, *sh))
+        zeroed = np.where((ids >= lo) & (ids < hi), scales, 0.0)
+        np.testing.assert_allclose(parts[-1], oracle.forward(x, ids, zeroed, w13, w2, *sh),
+                                   rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(sum(parts), full, rtol=1e-12, atol=1e-12)
+
+
 def test_empty_and_degenerate():
     ids, sc = oracle.route(np.zeros((0, 8), np.float32), RENORMALIZE_NAIVE, 2)
     assert ids.shape == (0, 2) and sc.shape == (0, 2)
