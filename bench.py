@@ -282,6 +282,37 @@ def run_ours(args, rank, world):
     kern_ms = {n: statistics.median([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(reps)])
                for j, n in enumerate(names)}
 
+    peaks_early, _ = load_peaks()
+    # ---- the router gate (logits = x . wg^T; with a shared expert its gate is fused in as
+    # one more row), not part of the timed step (the step takes the logits as input):
+    # timed on this workload's x with a seeded N(0, H^-1/2) gate matrix.
+    n_sh = 1 if w.shared_I else 0
+    wg = (torch.randn(w.E + n_sh, w.H, generator=torch.Generator(device=dev).manual_seed(7),
+                      device=dev) * w.H ** -0.5).to(torch.bfloat16)
+    lg_g = torch.empty((w.T, w.E), dtype=torch.float32, device=dev)
+    sg_g = torch.empty((w.T,), dtype=torch.float32, device=dev) if n_sh else None
+    for _ in range(3):
+        moe.moe_gate(x, wg, w.E, lg_g, sg_g, stream=stream)
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(20_000_000)
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        gev[i][0].record(stream)
+        moe.moe_gate(x, wg, w.E, lg_g, sg_g, stream=stream)
+        gev[i][1].record(stream)
+    torch.cuda.synchronize()
+    gate_ms = statistics.median(a.elapsed_time(b) for a, b in gev)
+    g_flops = 2.0 * w.T * w.H * (w.E + n_sh)
+    g_bytes = 2.0 * (w.T + w.E + n_sh) * w.H + 4.0 * w.T * (w.E + n_sh)
+    g_tc = g_flops / (peaks_early["bf16_tflops"] * 1e12) >= g_bytes / (peaks_early["hbm_gbs"] * 1e9)
+    gate = {"ms": round(gate_ms, 4), "rows": w.E + n_sh, "bound": "tensor" if g_tc else "hbm",
+            "achieved": round((g_flops / 1e12 if g_tc else g_bytes / 1e9) / (gate_ms * 1e-3), 1),
+            "unit": "TFLOP/s" if g_tc else "GB/s"}
+    gate["frac"] = round(gate["achieved"] / (peaks_early["bf16_tflops"] if g_tc else
+                                            peaks_early["hbm_gbs"]), 4)
+
     # ---- end to end through the public API: every step copies its inputs (x, logits)
     # in from pinned host memory and its result (y) out to pinned host memory. Three
     # streams and two device buffer sets let step i's copy-out and step i+1's copy-in run
@@ -387,6 +418,7 @@ def run_ours(args, rank, world):
         "roofline": roofline, "layer_roofline": layer,
         "kernels_ms": {n: round(v, 4) for n, v in kern_ms.items()},
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+        "gate_kernel": gate,
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, host_inputs(inp))

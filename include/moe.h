@@ -209,6 +209,19 @@ moe_status moe_forward_static(const moe_problem* p, const void* x, const int32_t
                               const float* scales, const void* w13, const void* w2,
                               const void* w13_s, const void* w2_s, void* y, void* stream);
 
+/* Router gate (vLLM MoE page, section "Gate 计算与 FSE"): router logits = x . wg^T with
+ * fp32 accumulation, one GEMM for the routed experts' gate and, with n_shared = 1, the
+ * fused shared-expert gate (FSE: wg is [E + 1, H], its last row the shared expert's gate).
+ *   x              device bf16 [T, H]
+ *   wg             device bf16 [E + n_shared, H]
+ *   routed_logits  device fp32 [T, E]: the logits moe_route takes
+ *   shared_logits  device fp32 [T] when n_shared = 1 (moe_forward_partial's shared_gate),
+ *                  else ignored (may be NULL)
+ * Requires H % 64 == 0 (64..32768), 1 <= E <= 256, n_shared in {0, 1}; 16-byte aligned
+ * pointers. Deterministic: partial sums over K are added in a fixed order. */
+moe_status moe_gate(const void* x, const void* wg, int64_t T, int32_t H, int32_t E,
+                    int32_t n_shared, float* routed_logits, float* shared_logits, void* stream);
+
 /* moe_forward restricted to the experts [e_lo, e_hi) of this call: the expert-parallel
  * seam of the TensorRT-LLM MoE page, section on supports_finalize_before_combine ("finalize
  * before combine": the top-k weighted sum taken on a rank's own rows, slots of other
@@ -218,11 +231,15 @@ moe_status moe_forward_static(const moe_problem* p, const void* x, const int32_t
  * The y of calls over a partition of [0, E) (the shared expert in exactly one of them) add
  * up to moe_forward's y. w13 / w2 hold the local experts only: [e_hi - e_lo, 2I, H] and
  * [e_hi - e_lo, H, I], expert g at plane g - e_lo. Requires 0 <= e_lo < e_hi <= E; ids in
- * [0, E) outside the range are not errors. moe_forward is this call with [0, E). */
+ * [0, E) outside the range are not errors. shared_gate: device fp32 [T] logits of the
+ * shared expert's gate (vLLM MoE page, "Gate 计算与 FSE": the shared expert's activation,
+ * a sigmoid), so that it enters with weight sigmoid(shared_gate[t]); NULL = weight 1.
+ * moe_forward is this call with [0, E) and no shared gate. */
 moe_status moe_forward_partial(const moe_problem* p, int32_t e_lo, int32_t e_hi, const void* x,
                                const int32_t* ids, const float* scales, const void* w13,
-                               const void* w2, const void* w13_s, const void* w2_s, void* y,
-                               void* workspace, size_t ws_bytes, void* stream);
+                               const void* w2, const void* w13_s, const void* w2_s,
+                               const float* shared_gate, void* y, void* workspace,
+                               size_t ws_bytes, void* stream);
 
 /* Step entry points (the kernels moe_forward runs, one at a time). Each takes the
  * same workspace; later steps read what earlier ones wrote into it. */

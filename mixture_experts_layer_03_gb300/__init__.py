@@ -71,7 +71,9 @@ _SIGS = {
                                           _P, _P]),
     "moe_forward_partial": (ctypes.c_int, [ctypes.POINTER(MoeProblem), ctypes.c_int32,
                                            ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                                           ctypes.c_size_t, _P]),
+                                           _P, ctypes.c_size_t, _P]),
+    "moe_gate": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                ctypes.c_int32, _P, _P, _P]),
     "moe_permute": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_fc1": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_fc2": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
@@ -225,11 +227,12 @@ def moe_forward(x, ids, scales, w13, w2, w13_s=None, w2_s=None, y=None,
 
 
 def moe_forward_partial(x, ids, scales, w13_local, w2_local, e_lo: int, e_hi: int, num_experts: int,
-                        w13_s=None, w2_s=None, y=None, workspace: Optional[Workspace] = None,
-                        stream=None):
+                        w13_s=None, w2_s=None, shared_gate=None, y=None,
+                        workspace: Optional[Workspace] = None, stream=None):
     """moe_forward over the experts [e_lo, e_hi) of num_experts only (the expert-parallel
     seam): slots routed elsewhere contribute 0. w13_local / w2_local hold those experts'
-    weights, [e_hi - e_lo, 2I, H] / [e_hi - e_lo, H, I]. Returns y bf16 [T, H]."""
+    weights, [e_hi - e_lo, 2I, H] / [e_hi - e_lo, H, I]. shared_gate: fp32 [T] logits that
+    weight the shared expert by their sigmoid (None: weight 1). Returns y bf16 [T, H]."""
     _cuda(x, "x", torch.bfloat16)
     _cuda(ids, "ids", torch.int32)
     _cuda(scales, "scales", torch.float32)
@@ -244,11 +247,33 @@ def moe_forward_partial(x, ids, scales, w13_local, w2_local, e_lo: int, e_hi: in
         workspace = alloc_workspace(p, x.device)
     if y is None:
         y = torch.empty_like(x)
+    if shared_gate is not None:
+        _cuda(shared_gate, "shared_gate", torch.float32)
     _check(_lib.moe_forward_partial(ctypes.byref(p), int(e_lo), int(e_hi), _ptr(x), _ptr(ids),
                                     _ptr(scales), _ptr(w13_local), _ptr(w2_local), _ptr(w13_s),
-                                    _ptr(w2_s), _ptr(y), workspace.ptr, workspace.nbytes,
-                                    _stream(stream)), "moe_forward_partial")
+                                    _ptr(w2_s), _ptr(shared_gate), _ptr(y), workspace.ptr,
+                                    workspace.nbytes, _stream(stream)), "moe_forward_partial")
     return y
+
+
+def moe_gate(x, wg, num_experts: int, routed_logits=None, shared_logits=None, stream=None):
+    """Router gate: x bf16 [T, H] . wg bf16 [E (+1), H]^T -> (routed logits fp32 [T, E],
+    shared-expert gate logits fp32 [T] or None). A wg with E + 1 rows carries the fused
+    shared-expert gate in its last row."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(wg, "wg", torch.bfloat16)
+    T, H = x.shape
+    E = int(num_experts)
+    n_shared = wg.shape[0] - E
+    if n_shared not in (0, 1) or wg.shape[1] != H:
+        raise ValueError(f"wg must be [{E} or {E + 1}, {H}], got {tuple(wg.shape)}")
+    if routed_logits is None:
+        routed_logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    if n_shared and shared_logits is None:
+        shared_logits = torch.empty((T,), dtype=torch.float32, device=x.device)
+    _check(_lib.moe_gate(_ptr(x), _ptr(wg), T, H, E, n_shared, _ptr(routed_logits),
+                         _ptr(shared_logits) if n_shared else None, _stream(stream)), "moe_gate")
+    return routed_logits, (shared_logits if n_shared else None)
 
 
 MOE_STATIC_SCRATCH_BYTES = 32 << 20

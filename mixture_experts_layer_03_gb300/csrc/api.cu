@@ -236,14 +236,31 @@ moe_status moe_finalize(const moe_problem* p, const float* scales, void* y, void
   if (st != MOE_OK || p->T == 0) return st;
   if (!scales || !y || !aligned16(scales) || !aligned16(y))
     return set_error(MOE_ERR_INVALID_ARG, "scales/y NULL or not 16-byte aligned");
-  return launch_finalize(*p, L, scales, y, static_cast<const char*>(workspace),
+  return launch_finalize(*p, L, scales, nullptr, y, static_cast<const char*>(workspace),
                          static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_gate(const void* x, const void* wg, int64_t T, int32_t H, int32_t E,
+                    int32_t n_shared, float* routed_logits, float* shared_logits, void* stream) {
+  if (T < 0 || T > (int64_t{1} << 31) / 8 || H < 64 || H % 64 != 0 || H > 32768 || E < 1 ||
+      E > 256 || n_shared < 0 || n_shared > 1)
+    return set_error(MOE_ERR_UNSUPPORTED, "gate shape outside the envelope (T %lld, H %d, E %d, "
+                     "n_shared %d)", static_cast<long long>(T), H, E, n_shared);
+  if (T == 0) return MOE_OK;
+  if (!x || !wg || !routed_logits || (n_shared == 1 && !shared_logits))
+    return set_error(MOE_ERR_INVALID_ARG, "NULL gate argument");
+  if (!aligned16(x) || !aligned16(wg) || !aligned16(routed_logits) ||
+      (shared_logits && !aligned16(shared_logits)))
+    return set_error(MOE_ERR_INVALID_ARG, "gate pointers must be 16-byte aligned");
+  return launch_gate(x, wg, T, H, E, n_shared, routed_logits, n_shared ? shared_logits : nullptr,
+                     nullptr, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_forward_partial(const moe_problem* p, int32_t e_lo, int32_t e_hi, const void* x,
                                const int32_t* ids, const float* scales, const void* w13,
-                               const void* w2, const void* w13_s, const void* w2_s, void* y,
-                               void* workspace, size_t ws_bytes, void* stream) {
+                               const void* w2, const void* w13_s, const void* w2_s,
+                               const float* shared_gate, void* y, void* workspace,
+                               size_t ws_bytes, void* stream) {
   moe_ws_layout L;
   moe_status st = check_forward_common(p, workspace, ws_bytes, &L);
   if (st != MOE_OK || p->T == 0) return st;
@@ -261,14 +278,14 @@ moe_status moe_forward_partial(const moe_problem* p, int32_t e_lo, int32_t e_hi,
   if ((st = launch_permute(*p, L, x, ids, e_lo, e_hi, ws, s)) != MOE_OK) return st;
   if ((st = launch_fc1(*p, L, w13, w13_s, e_lo, e_hi, ws, s)) != MOE_OK) return st;
   if ((st = launch_fc2(*p, L, w2, w2_s, e_lo, e_hi, ws, s)) != MOE_OK) return st;
-  return launch_finalize(*p, L, scales, y, ws, s);
+  return launch_finalize(*p, L, scales, shared_gate, y, ws, s);
 }
 
 moe_status moe_forward(const moe_problem* p, const void* x, const int32_t* ids, const float* scales,
                        const void* w13, const void* w2, const void* w13_s, const void* w2_s, void* y,
                        void* workspace, size_t ws_bytes, void* stream) {
-  return moe_forward_partial(p, 0, p ? p->E : 0, x, ids, scales, w13, w2, w13_s, w2_s, y,
-                             workspace, ws_bytes, stream);
+  return moe_forward_partial(p, 0, p ? p->E : 0, x, ids, scales, w13, w2, w13_s, w2_s, nullptr,
+                             y, workspace, ws_bytes, stream);
 }
 
 }  // extern "C"
@@ -335,7 +352,7 @@ moe_status moe_forward_static(const moe_problem* p, const void* x, const int32_t
   if ((st = launch_permute(*p, L, x, ids, 0, p->E, ws, s)) != MOE_OK) return st;
   if ((st = launch_fc1(*p, L, w13, w13_s, 0, p->E, ws, s)) != MOE_OK) return st;
   if ((st = launch_fc2(*p, L, w2, w2_s, 0, p->E, ws, s)) != MOE_OK) return st;
-  return launch_finalize(*p, L, scales, y, ws, s);
+  return launch_finalize(*p, L, scales, nullptr, y, ws, s);
 }
 
 moe_status moe_read_device_status(void* workspace, void* stream, int32_t* flags) {

@@ -30,8 +30,8 @@ __device__ __forceinline__ void acc_row(float (&acc)[8], uint4 v, float s) {
 template <int K>
 __global__ void __launch_bounds__(kFinThreads)
 finalize_kernel(const __nv_bfloat16* __restrict__ out_perm, const int32_t* __restrict__ perm_inv,
-                const float* __restrict__ scales, int64_t T, int H, int64_t shared_row0,
-                __nv_bfloat16* __restrict__ y) {
+                const float* __restrict__ scales, const float* __restrict__ shared_gate, int64_t T,
+                int H, int64_t shared_row0, __nv_bfloat16* __restrict__ y) {
   constexpr int k = K;
   constexpr int kMaxK = K;
   pdl_trigger();
@@ -64,7 +64,11 @@ finalize_kernel(const __nv_bfloat16* __restrict__ out_perm, const int32_t* __res
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j)
       if (row[j] >= 0) acc_row(acc, val[j], sc[j]);
-    if (shared_row0 >= 0) acc_row(acc, shv, 1.0f);
+    if (shared_row0 >= 0) {
+      // Fused shared-expert gate (vLLM MoE page, "Gate 计算与 FSE"): sigmoid of its logit.
+      const float gs = shared_gate ? 1.0f / (1.0f + expf(-__ldg(shared_gate + t))) : 1.0f;
+      acc_row(acc, shv, gs);
+    }
     uint4 o;
     uint32_t* po = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
@@ -87,7 +91,7 @@ __global__ void cast_kernel(const float* __restrict__ in, __nv_bfloat16* __restr
 
 template <int K>
 cudaError_t launch_finalize_k(const moe_problem& p, const moe_ws_layout& L, const float* scales,
-                              void* y, const char* ws, cudaStream_t s) {
+                              const float* shared_gate, void* y, const char* ws, cudaStream_t s) {
   const int64_t P = p.T * p.k;
   const int64_t total = p.T * (p.H / 8);
   int64_t grid = (total + kFinThreads - 1) / kFinThreads;
@@ -95,24 +99,24 @@ cudaError_t launch_finalize_k(const moe_problem& p, const moe_ws_layout& L, cons
   if (grid > cap) grid = cap;
   return launch_pdl(finalize_kernel<K>, dim3(static_cast<unsigned>(grid)), dim3(kFinThreads), 0, s,
                     reinterpret_cast<const __nv_bfloat16*>(ws + L.out_perm),
-                    reinterpret_cast<const int32_t*>(ws + L.perm_inv), scales, p.T, p.H,
+                    reinterpret_cast<const int32_t*>(ws + L.perm_inv), scales, shared_gate, p.T, p.H,
                     static_cast<int64_t>(p.shared_I > 0 ? P : -1), static_cast<__nv_bfloat16*>(y));
 }
 
 }  // namespace
 
 moe_status launch_finalize(const moe_problem& p, const moe_ws_layout& L, const float* scales,
-                           void* y, const char* ws, cudaStream_t s) {
+                           const float* shared_gate, void* y, const char* ws, cudaStream_t s) {
   cudaError_t err;
   switch (p.k) {
-    case 1: err = launch_finalize_k<1>(p, L, scales, y, ws, s); break;
-    case 2: err = launch_finalize_k<2>(p, L, scales, y, ws, s); break;
-    case 3: err = launch_finalize_k<3>(p, L, scales, y, ws, s); break;
-    case 4: err = launch_finalize_k<4>(p, L, scales, y, ws, s); break;
-    case 5: err = launch_finalize_k<5>(p, L, scales, y, ws, s); break;
-    case 6: err = launch_finalize_k<6>(p, L, scales, y, ws, s); break;
-    case 7: err = launch_finalize_k<7>(p, L, scales, y, ws, s); break;
-    default: err = launch_finalize_k<8>(p, L, scales, y, ws, s); break;
+    case 1: err = launch_finalize_k<1>(p, L, scales, shared_gate, y, ws, s); break;
+    case 2: err = launch_finalize_k<2>(p, L, scales, shared_gate, y, ws, s); break;
+    case 3: err = launch_finalize_k<3>(p, L, scales, shared_gate, y, ws, s); break;
+    case 4: err = launch_finalize_k<4>(p, L, scales, shared_gate, y, ws, s); break;
+    case 5: err = launch_finalize_k<5>(p, L, scales, shared_gate, y, ws, s); break;
+    case 6: err = launch_finalize_k<6>(p, L, scales, shared_gate, y, ws, s); break;
+    case 7: err = launch_finalize_k<7>(p, L, scales, shared_gate, y, ws, s); break;
+    default: err = launch_finalize_k<8>(p, L, scales, shared_gate, y, ws, s); break;
   }
   if (err != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "finalize launch: %s", cudaGetErrorString(err));

@@ -1,0 +1,267 @@
+// Router gate (vLLM MoE page, section "Gate 计算与 FSE"): router_logits = x . wg^T, one
+// GEMM for the routed experts' gate and, with the fused shared-expert gate (FSE), the
+// shared expert's gate as one more row of wg ([E + n_shared, H]).
+//
+// The contraction is long in K (H) and small in M x N (T x (E + n_shared)), so a tile of
+// 128 tokens x up to 256 gate rows is split along K over the S CTAs of a thread-block
+// cluster: each CTA runs tcgen05 MMAs (operands staged by TMA, fp32 accumulator in TMEM)
+// over its share of the K blocks, copies its partial tile into its own shared memory,
+// and after a cluster barrier reduces 128 / S of the tile's rows over the S partials
+// (read through distributed shared memory) in rank order, so the sums are deterministic.
+// Rows past T and columns past E + n_shared are zero-filled by the tensor maps and not
+// stored.
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "launch.cuh"
+#include "ptx.cuh"
+#include "tmap.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kGateBK = 64;                  // K elements per stage
+constexpr int kGateRowBytes = kGateBK * 2;
+constexpr int kGateMaxStages = 8;
+constexpr int kGateXBytes = 128 * kGateRowBytes;       // 128 token rows
+constexpr int kGateWMaxBytes = 256 * kGateRowBytes;    // up to 256 gate rows
+constexpr int kGateRingBytes = 4 * (kGateXBytes + kGateWMaxBytes);   // 192 KB of stages
+constexpr int kGateSmemBytes = 1024 + kGateRingBytes;
+constexpr int kGateMaxSplit = 8;             // portable cluster size
+static_assert(kGateBK == static_cast<int>(kMapBoxCols), "tensor-map boxes are one K block wide");
+
+struct GateArgs {
+  int64_t T;
+  int H;
+  int E;            // routed gate rows
+  int E_out;        // E + n_shared
+  int n_col;        // column tiles of 256
+  int S;            // CTAs per cluster (K split)
+  int box_rows;     // gate rows per tensor-map box (min(256, round_up(E_out, 16)))
+  int stage_bytes;  // X box + W box, rounded up to 1024 (the swizzle atom)
+  int stages;       // ring depth: as many stages as fit in the ring, at most 8
+  uint32_t tmem_cols;
+  float* logits;          // [T, E]
+  float* shared_logits;   // [T] or NULL
+  int32_t* status;        // device status word or NULL
+};
+
+__global__ void __launch_bounds__(128, 1)
+gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+            GateArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[kGateMaxStages], empty_bar[kGateMaxStages], acc_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int S = g.S;
+  const uint32_t rank = cluster_ctarank();
+  const int cluster = static_cast<int>(blockIdx.x) / S;
+  const int col_tile = cluster % g.n_col;
+  const int row_tile = cluster / g.n_col;
+  const int col0 = col_tile * 256;
+  const int n_cols = min(256, g.E_out - col0);
+  const int n_mma = (n_cols + 15) & ~15;
+  const int row0 = row_tile * 128;
+  const int nkb = g.H / kGateBK;
+  const int kb0 = static_cast<int>(rank) * nkb / S;
+  const int kb1 = (static_cast<int>(rank) + 1) * nkb / S;
+
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  float* partial = reinterpret_cast<float*>(smem);   // [128][n_mma + 4], after the MMAs
+  const int pstride = n_mma + 4;
+
+  pdl_trigger();
+  if (tid == 0) {
+    for (int s = 0; s < g.stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&acc_bar, 1);
+    s_abort = 0;
+    fence_barrier_init();
+    tma_prefetch_map(&map_x);
+    tma_prefetch_map(&map_w);
+  }
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, g.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort = &s_abort;
+  pdl_wait();   // x may be the previous kernel's output
+
+  if (warp == 0 && lane == 0) {
+    // TMA producer over this CTA's K blocks.
+    const uint32_t bytes = static_cast<uint32_t>(kGateXBytes + g.box_rows * kGateRowBytes);
+    int issued = 0;
+    for (int kb = kb0; kb < kb1; ++kb, ++issued) {
+      const int st = issued % g.stages;
+      if (!mbar_wait(&empty_bar[st], ((issued / g.stages) & 1) ^ 1u, abort)) {
+        *abort = 1;
+        break;
+      }
+      mbar_arrive_expect_tx(&full_bar[st], bytes);
+      uint8_t* xs = smem + st * g.stage_bytes;
+      tma_load_2d(xs, &map_x, &full_bar[st], kb * kGateBK, row0);
+      tma_load_2d(xs + kGateXBytes, &map_w, &full_bar[st], kb * kGateBK, col0);
+    }
+    if (*abort) {
+      // Let the copies in flight land before shared memory is reused (bounded waits).
+      volatile int never = 0;
+      const int first = issued > g.stages ? issued - g.stages : 0;
+      for (int i = first; i < issued; ++i)
+        mbar_wait(&full_bar[i % g.stages], (i / g.stages) & 1, &never);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer: D[128 tokens, n_mma gate rows] += X . W^T.
+    const uint32_t idesc = idesc_bf16_f32(128, n_mma);
+    for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
+      const int st = i % g.stages;
+      if (!mbar_wait(&full_bar[st], (i / g.stages) & 1, abort)) {
+        *abort = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t xa = smem_u32(smem + st * g.stage_bytes);
+      const uint32_t wa = xa + kGateXBytes;
+#pragma unroll
+      for (int kk = 0; kk < kGateBK / 16; ++kk)
+        umma_bf16(tmem, sdesc_k_major(xa + kk * 32, kGateRowBytes),
+                  sdesc_k_major(wa + kk * 32, kGateRowBytes), idesc, (i | kk) != 0);
+      umma_commit(&empty_bar[st]);
+    }
+    umma_commit(&acc_bar);   // arrives once every MMA issued above has completed
+  }
+  __syncwarp();
+
+  // Partial tile: TMEM lane (token row) 32 * warp + lane, columns 0..n_mma-1.
+  const bool done = mbar_wait(&acc_bar, 0, abort);
+  if (!__all_sync(0xffffffffu, done)) *abort = 1;
+  tc_fence_after();
+  {
+    const int row = 32 * warp + lane;
+    float v[16];
+    for (int c0 = 0; c0 < n_mma; c0 += 16) {
+      tmem_ld_x16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + c0, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) partial[row * pstride + c0 + i] = v[i];
+    }
+  }
+  tc_fence_before();
+  cluster_sync();   // every CTA's partial tile is in its shared memory
+
+  // This CTA's rows of the tile, summed over the S partials in rank order: four columns
+  // per thread and step, the S partials' loads issued before the adds.
+  const int r0 = static_cast<int>(rank) * 128 / S, r1 = (static_cast<int>(rank) + 1) * 128 / S;
+  const uint32_t pbase = smem_u32(partial);
+  const int nq = n_mma / 4;   // column quads of the partial tile
+  for (int idx = tid; idx < (r1 - r0) * nq; idx += blockDim.x) {
+    const int row = r0 + idx / nq;
+    const int col = (idx - (row - r0) * nq) * 4;
+    const uint32_t off = static_cast<uint32_t>((row * pstride + col) * 4);
+    float4 part[kGateMaxSplit];
+#pragma unroll
+    for (int q = 0; q < kGateMaxSplit; ++q)
+      if (q < S) part[q] = ld_shared_cluster_f32x4(mapa_shared(pbase + off, q));
+    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < kGateMaxSplit; ++q)
+      if (q < S) {
+        sum[0] += part[q].x;
+        sum[1] += part[q].y;
+        sum[2] += part[q].z;
+        sum[3] += part[q].w;
+      }
+    const int64_t t = row0 + row;
+    if (t < g.T) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = col0 + col + j;
+        if (col + j >= n_cols) break;
+        if (c < g.E) g.logits[t * g.E + c] = sum[j];
+        else if (g.shared_logits) g.shared_logits[t] = sum[j];
+      }
+    }
+  }
+  cluster_sync();   // no CTA leaves while another reads its shared memory
+  if (tid == 0 && *abort && g.status) atomicOr(g.status, MOE_DEVICE_FLAG_TIMEOUT);
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, g.tmem_cols);
+  }
+}
+
+}  // namespace
+
+moe_status launch_gate(const void* x, const void* wg, int64_t T, int H, int E, int n_shared,
+                       float* logits, float* shared_logits, int32_t* status, cudaStream_t s) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_done[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGateSmemBytes);
+    if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "gate smem attribute: %s", cudaGetErrorString(e));
+    attr_done[dev] = true;
+  }
+  GateArgs g;
+  g.T = T;
+  g.H = H;
+  g.E = E;
+  g.E_out = E + n_shared;
+  g.n_col = (g.E_out + 255) / 256;
+  const int n_row = static_cast<int>((T + 127) / 128);
+  const int nkb = H / kGateBK;
+  // Enough CTAs to cover the SMs, at least two K blocks each, at most the portable cluster.
+  const int clusters = n_row * g.n_col;
+  const int want = (device_sm_count() + clusters - 1) / clusters;
+  int S = 1;   // a power of two: 1, 2, 4 or 8 CTAs per cluster
+  while (S * 2 <= want && S * 2 <= kGateMaxSplit && S * 2 <= nkb / 2) S *= 2;
+  g.S = S;
+  const int e16 = (g.E_out + 15) & ~15;
+  g.box_rows = e16 < 256 ? e16 : 256;
+  g.stage_bytes = (kGateXBytes + g.box_rows * kGateRowBytes + 1023) & ~1023;
+  g.stages = kGateRingBytes / g.stage_bytes;
+  if (g.stages > kGateMaxStages) g.stages = kGateMaxStages;
+  uint32_t cols = 32;
+  while (cols < static_cast<uint32_t>(g.box_rows)) cols <<= 1;
+  g.tmem_cols = cols;
+  g.logits = logits;
+  g.shared_logits = shared_logits;
+  g.status = status;
+  CUtensorMap mx, mw;
+  if (!encode_map2(&mx, x, static_cast<uint64_t>(T), static_cast<uint64_t>(H), 128) ||
+      !encode_map2(&mw, wg, static_cast<uint64_t>(g.E_out), static_cast<uint64_t>(H),
+                   static_cast<uint32_t>(g.box_rows)))
+    return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (gate)");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * S));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = kGateSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, gate_kernel, mx, mw, g);
+  if (err != cudaSuccess) return set_error(MOE_ERR_CUDA, "gate launch: %s", cudaGetErrorString(err));
+  return MOE_OK;
+}
+
+}  // namespace moe

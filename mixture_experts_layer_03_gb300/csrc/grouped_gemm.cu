@@ -49,11 +49,13 @@
 #include "internal.h"
 #include "launch.cuh"
 #include "ptx.cuh"
+#include "tmap.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kBK = 64;                              // K elements per stage
+static_assert(kBK == static_cast<int>(kMapBoxCols), "tensor-map boxes are one K block wide");
 constexpr int kRowBytes = kBK * 2;                   // one K row of a tile = the swizzle width
 constexpr int kXStageBytes = 128 * kRowBytes;        // 128 rows of X
 constexpr int kWStageBytes = 128 * kRowBytes;        // 128 rows of W
@@ -941,56 +943,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
 
 // ---------------------------------------------------------------- host side
 
-constexpr CUtensorMapSwizzle kSwizzle =
-    kRowBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
-// bf16 matrix [rows, cols] (cols contiguous), box = kBK cols x box_rows rows.
-bool encode_map2(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                 uint32_t box_rows) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {kBK, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, kSwizzle,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// bf16 tensor [planes, rows, cols] (cols contiguous), box = kBK cols x box_rows rows x 1.
-bool encode_map3(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t cols,
-                 uint32_t box_rows) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {cols, rows, planes};
-  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
-  cuuint32_t box[3] = {kBK, box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, kSwizzle,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
 
 // Per device: the large dynamic shared memory opt-in of both kernels, and how many 2-CTA
 // clusters of the pair kernel can be resident at once.

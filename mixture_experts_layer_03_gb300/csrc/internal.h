@@ -55,8 +55,12 @@ moe_status launch_fc1(const moe_problem& p, const moe_ws_layout& L, const void* 
 moe_status launch_fc2(const moe_problem& p, const moe_ws_layout& L, const void* w2,
                       const void* w2_s, int e_lo, int e_hi, char* ws, cudaStream_t s);
 
+// shared_gate: fp32 [T] gate logits of the shared expert (weight sigmoid) or NULL (1).
 moe_status launch_finalize(const moe_problem& p, const moe_ws_layout& L, const float* scales,
-                           void* y, const char* ws, cudaStream_t s);
+                           const float* shared_gate, void* y, const char* ws, cudaStream_t s);
+
+moe_status launch_gate(const void* x, const void* wg, int64_t T, int H, int E, int n_shared,
+                       float* logits, float* shared_logits, int32_t* status, cudaStream_t s);
 
 moe_status launch_cast_f32_bf16(const float* in, void* out, int64_t n, cudaStream_t s);
 

@@ -5,11 +5,11 @@ baseline / reference arm; never by the product path.
 """
 from .moe_oracle import (DEFAULT, RENORMALIZE, DEEPSEEKV3, LLAMA4, RENORMALIZE_NAIVE, MINIMAX2,
                          SIGMOID_RENORM, METHODS, topk_desc, softmax64, sigmoid64, deepseek_keys, group_select,
-                         route, permute, swiglu, expert_ffn, forward, forward_partial,
+                         route, permute, swiglu, expert_ffn, gate, forward, forward_partial,
                          forward_permuted)
 
 __all__ = ["DEFAULT", "RENORMALIZE", "DEEPSEEKV3", "LLAMA4", "RENORMALIZE_NAIVE", "MINIMAX2",
            "SIGMOID_RENORM",
            "METHODS", "topk_desc", "softmax64", "sigmoid64", "deepseek_keys", "group_select",
-           "route", "permute", "swiglu", "expert_ffn", "forward", "forward_partial",
+           "route", "permute", "swiglu", "expert_ffn", "gate", "forward", "forward_partial",
            "forward_permuted"]

@@ -209,8 +209,28 @@ def expert_ffn(X: np.ndarray, w13e, w2e) -> np.ndarray:
     return h @ w2e.T
 
 
-def forward(x, ids, scales, w13, w2, w13_s=None, w2_s=None) -> np.ndarray:
-    """y [T, H] float64 = sum_j scales[t, j] * E_{ids[t, j]}(x[t]) (+ shared(x[t])).
+def gate(x, wg, num_experts: int):
+    """Router gate: logits = x . wg^T in float64. VLLM, section "Gate 计算与 FSE": with the
+    fused shared-expert gate, wg has E + 1 rows and its last row gives the shared expert's
+    gate logit. Returns (routed logits [T, E], shared logits [T] or None)."""
+    X = np.asarray(x, dtype=np.float64)
+    W = np.asarray(wg, dtype=np.float64)
+    out = X @ W.T
+    E = int(num_experts)
+    return out[:, :E], (out[:, E] if W.shape[0] > E else None)
+
+
+def _shared_weight(shared_gate, T):
+    """Weight of the shared expert per token: 1, or sigmoid of its gate logit (VLLM, section
+    "Gate 计算与 FSE": the shared expert's activation is usually a sigmoid)."""
+    if shared_gate is None:
+        return np.ones((T, 1))
+    return sigmoid64(np.asarray(shared_gate, dtype=np.float64))[:, None]
+
+
+def forward(x, ids, scales, w13, w2, w13_s=None, w2_s=None, shared_gate=None) -> np.ndarray:
+    """y [T, H] float64 = sum_j scales[t, j] * E_{ids[t, j]}(x[t]) (+ g_t * shared(x[t]),
+    g_t = 1 or sigmoid(shared_gate[t])).
 
     ``w13``/``w2`` are indexable per expert (``w13[e]`` -> [2I, H]), so callers can
     hand over one expert at a time. Tokens are independent: passing a subset of
@@ -226,12 +246,12 @@ def forward(x, ids, scales, w13, w2, w13_s=None, w2_s=None) -> np.ndarray:
         o = expert_ffn(X[rows], w13[int(e)], w2[int(e)])
         np.add.at(y, rows, scales[rows, slots][:, None] * o)
     if w13_s is not None:
-        y += expert_ffn(X, w13_s, w2_s)
+        y += _shared_weight(shared_gate, T) * expert_ffn(X, w13_s, w2_s)
     return y
 
 
 def forward_partial(x, ids, scales, w13_local, w2_local, e_lo: int, e_hi: int, w13_s=None,
-                    w2_s=None) -> np.ndarray:
+                    w2_s=None, shared_gate=None) -> np.ndarray:
     """The layer restricted to the experts [e_lo, e_hi): the slots whose expert lies
     there, weighted by their scales (+ the shared expert when given).
 
@@ -251,7 +271,7 @@ def forward_partial(x, ids, scales, w13_local, w2_local, e_lo: int, e_hi: int, w
         o = expert_ffn(X[rows], w13_local[e - e_lo], w2_local[e - e_lo])
         np.add.at(y, rows, scales[rows, slots][:, None] * o)
     if w13_s is not None:
-        y += expert_ffn(X, w13_s, w2_s)
+        y += _shared_weight(shared_gate, T) * expert_ffn(X, w13_s, w2_s)
     return y
 
 

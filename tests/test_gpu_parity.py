@@ -283,6 +283,56 @@ def test_forward_partial_over_a_partition(moe, T, H, I, E, k, sI, cuts):
                  "sum of the partials vs moe_forward")
 
 
+GATE_TOL = 1e-4   # fp32 accumulation of H bf16 products, relative to max|logit|
+
+
+@pytest.mark.parametrize("T,H,E,ns,method", [
+    (300, 256, 8, 0, RENORMALIZE_NAIVE),      # one column tile, ragged last row tile
+    (513, 1024, 256, 1, DEEPSEEKV3),          # FSE: 257 gate rows -> two column tiles
+    (64, 2048, 128, 0, RENORMALIZE_NAIVE),    # decode size: one row tile split along K
+    (1, 128, 16, 1, LLAMA4),                  # a single token
+    (4096, 4096, 8, 0, RENORMALIZE_NAIVE),    # mixtral_prefill's gate
+    (100, 512, 2, 1, RENORMALIZE_NAIVE),      # 3 gate rows (padded to 4), FSE row last
+    (77, 256, 15, 1, RENORMALIZE_NAIVE),      # 16 rows, one 16-row MMA tile
+])
+def test_gate_parity_and_routing_on_its_logits(moe, T, H, E, ns, method):
+    g = torch.Generator().manual_seed(T + E)
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    wg = (torch.randn(E + ns, H, generator=g) * H ** -0.5).to(torch.bfloat16)
+    lg, sg = moe.moe_gate(x.cuda(), wg.cuda(), E)
+    lg2, _ = moe.moe_gate(x.cuda(), wg.cuda(), E)
+    torch.cuda.synchronize()
+    assert torch.equal(lg, lg2)   # fixed reduction order
+    ref_r, ref_s = oracle.gate(_np64(x), _np64(wg), E)
+    _check_close(lg.cpu().double().numpy(), ref_r, GATE_TOL, "routed logits")
+    if ns:
+        _check_close(sg.cpu().double().numpy(), ref_s, GATE_TOL, "shared gate logits")
+    else:
+        assert sg is None
+    # The routing decision is taken on the same fp32 logits on both sides.
+    k = 1 if method == LLAMA4 else min(8, E)
+    kw = dict(n_group=8, topk_group=4, routed_scaling_factor=2.5) if method == DEEPSEEKV3 else {}
+    ids, sc = moe.moe_route(lg, method, k, **kw)
+    ids_ref, sc_ref = oracle.route(lg.cpu().numpy(), method, k, **kw)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(sc.cpu().numpy(), sc_ref, rtol=1e-6, atol=0)
+
+
+def test_forward_with_the_fused_shared_gate(moe):
+    T, H, I, E, k, sI = 300, 256, 192, 8, 2, 128
+    c = _random_case(T, H, I, E, k, sI, seed=5)
+    dev = {n: (None if v is None else (torch.from_numpy(v) if isinstance(v, np.ndarray) else v).cuda())
+           for n, v in c.items()}
+    sg = torch.randn(T, generator=torch.Generator().manual_seed(6)) * 2.0
+    y = moe.moe_forward_partial(dev["x"], dev["ids"], dev["sc"], dev["w13"], dev["w2"], 0, E, E,
+                                dev["w13s"], dev["w2s"], shared_gate=sg.cuda())
+    torch.cuda.synchronize()
+    ref = oracle.forward(_np64(c["x"]), c["ids"], c["sc"], ExpertView(c["w13"]),
+                         ExpertView(c["w2"]), _np64(c["w13s"]), _np64(c["w2s"]),
+                         shared_gate=sg.double().numpy())
+    _check_close(y.cpu().double().numpy(), ref, Y_TOL, "y with the shared gate")
+
+
 def test_forward_is_deterministic(moe):
     c = _random_case(2000, 256, 256, 16, 4, 0, seed=3)
     _, ws, y1, dev = _run_forward_steps(moe, c)

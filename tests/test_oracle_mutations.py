@@ -120,3 +120,12 @@ def test_partial_ignoring_scales_is_caught(monkeypatch):
     monkeypatch.setattr(om, "forward_partial", bad_partial)
     monkeypatch.setattr(oracle, "forward_partial", bad_partial)
     _fails(pins.test_partial_forward_partition_and_zeroed_scales)
+
+
+def test_shared_gate_without_sigmoid_is_caught(monkeypatch):
+    def bad_weight(shared_gate, T):
+        if shared_gate is None:
+            return np.ones((T, 1))
+        return np.asarray(shared_gate, dtype=np.float64)[:, None]
+    monkeypatch.setattr(om, "_shared_weight", bad_weight)
+    _fails(pins.test_shared_gate_weight_limits_and_linearity)

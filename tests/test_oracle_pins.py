@@ -404,6 +404,47 @@ def test_partial_forward_partition_and_zeroed_scales():
     np.testing.assert_allclose(sum(parts), full, rtol=1e-12, atol=1e-12)
 
 
+def test_gate_is_the_plain_product_and_splits_the_shared_row():
+    rng = np.random.default_rng(10)
+    T, H, E = 5, 7, 4
+    x = rng.standard_normal((T, H))
+    wg = rng.standard_normal((E + 1, H))
+    routed, shared = oracle.gate(x, wg, E)
+    for t in range(T):
+        for e in range(E + 1):
+            want = sum(x[t, h] * wg[e, h] for h in range(H))
+            got = routed[t, e] if e < E else shared[t]
+            assert abs(got - want) <= 1e-12 * max(1.0, abs(want))
+    r2, s2 = oracle.gate(x, wg[:E], E)
+    assert s2 is None and np.array_equal(r2, routed)
+
+
+def test_shared_gate_weight_limits_and_linearity():
+    """The fused shared-expert gate scales the shared expert by sigmoid(g): g -> +inf gives
+    the ungated layer, g -> -inf the routed part alone, and in between the layer is
+    routed + sigmoid(g) * (ungated - routed)."""
+    rng = np.random.default_rng(11)
+    T, H, I, E, k, Is = 6, 5, 4, 3, 2, 3
+    x = rng.standard_normal((T, H))
+    w13 = rng.standard_normal((E, 2 * I, H))
+    w2 = rng.standard_normal((E, H, I))
+    w13s = rng.standard_normal((2 * Is, H))
+    w2s = rng.standard_normal((H, Is))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    sc = rng.random((T, k))
+    ungated = oracle.forward(x, ids, sc, w13, w2, w13s, w2s)
+    routed = oracle.forward(x, ids, sc, w13, w2)
+    np.testing.assert_allclose(oracle.forward(x, ids, sc, w13, w2, w13s, w2s,
+                                              shared_gate=np.full(T, 60.0)), ungated, rtol=1e-12)
+    np.testing.assert_allclose(oracle.forward(x, ids, sc, w13, w2, w13s, w2s,
+                                              shared_gate=np.full(T, -60.0)), routed,
+                               rtol=1e-12, atol=1e-20)
+    g = rng.standard_normal(T)
+    sig = np.array([1 / (1 + math.exp(-v)) for v in g])[:, None]
+    np.testing.assert_allclose(oracle.forward(x, ids, sc, w13, w2, w13s, w2s, shared_gate=g),
+                               routed + sig * (ungated - routed), rtol=1e-12, atol=1e-12)
+
+
 def test_empty_and_degenerate():
     ids, sc = oracle.route(np.zeros((0, 8), np.float32), RENORMALIZE_NAIVE, 2)
     assert ids.shape == (0, 2) and sc.shape == (0, 2)
