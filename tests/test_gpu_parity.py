@@ -333,6 +333,32 @@ def test_forward_with_the_fused_shared_gate(moe):
     _check_close(y.cpu().double().numpy(), ref, Y_TOL, "y with the shared gate")
 
 
+@pytest.mark.parametrize("T,E,k", [(65536, 8, 8), (40000, 256, 8)])
+def test_largest_row_counts(moe, T, E, k):
+    """Many permuted rows (T*k up to 524,288): routing, the permutation and sampled y."""
+    H, I = 128, 64
+    g = torch.Generator(device="cuda").manual_seed(T)
+    logits = torch.randn(T, E, generator=g, device="cuda")
+    x = torch.randn(T, H, generator=g, device="cuda").to(torch.bfloat16)
+    w13 = (torch.randn(E, 2 * I, H, generator=g, device="cuda") * H ** -0.5).to(torch.bfloat16)
+    w2 = (torch.randn(E, H, I, generator=g, device="cuda") * I ** -0.5).to(torch.bfloat16)
+    ids, sc = moe.moe_route(logits, RENORMALIZE_NAIVE, k)
+    p = moe.make_problem(T, H, I, E, k)
+    ws = moe.alloc_workspace(p)
+    y = moe.moe_forward(x, ids, sc, w13, w2, workspace=ws)
+    torch.cuda.synchronize()
+    ids_ref, sc_ref = oracle.route(logits.cpu().numpy(), RENORMALIZE_NAIVE, k)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    counts, offsets, perm_src, perm_inv = oracle.permute(ids_ref, E)
+    assert np.array_equal(ws.region("perm_src", T * k, torch.int32).cpu().numpy(), perm_src)
+    sample = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(1).choice(T, 24, replace=False)]))
+    y_ref = oracle.forward(x[sample].cpu().double().numpy(), ids_ref[sample], sc_ref[sample],
+                           ExpertView(w13), ExpertView(w2))
+    _check_close(y[sample].cpu().double().numpy(), y_ref, Y_TOL, "y (sampled)")
+    st, flags = moe.moe_read_device_status(ws)
+    assert st == moe.MOE_OK and flags == 0
+
+
 def test_forward_is_deterministic(moe):
     c = _random_case(2000, 256, 256, 16, 4, 0, seed=3)
     _, ws, y1, dev = _run_forward_steps(moe, c)
