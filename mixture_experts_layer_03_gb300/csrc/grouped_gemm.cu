@@ -95,6 +95,7 @@ struct Unit {
   int row0;          // token-major: this CTA's first row; weight-major: the first leftover row
   int rows;          // valid rows (token-major 128; weight-major 1..255)
   int ntok;          // weight-major: rows rounded up to 16 (the MMA N)
+  int narrow;        // single-SM only: a narrow weight-major tile (128 weight rows)
   int n0;            // first output channel of the unit
   int K;
   int N;             // channels of this group
@@ -127,6 +128,7 @@ __device__ __forceinline__ Unit decode_unit(int unit, const int32_t* s_off, cons
   t.K = shared ? a.K_shared : a.K_routed;
   t.N = shared ? a.N_shared : a.N_routed;
   t.n0 = nt * (fc1 ? kFc1Cols : kFc2Cols);
+  t.narrow = 0;
   if (u < pairs || left > 128) {
     // Two row tiles, one per CTA; for the leftover unit (129..255 rows) the second tile
     // is partial and its missing rows are masked.
@@ -143,12 +145,28 @@ __device__ __forceinline__ Unit decode_unit(int unit, const int32_t* s_off, cons
   return t;
 }
 
-// Single-SM list: every row tile of a group with m < 256 (a full tile and/or the partial
-// last tile), channel-tile major.
+// Single-SM list: every row tile of a group (full 128-row tiles and/or the partial last
+// tile), channel-tile major; in a narrow launch a group of at most kNarrowRows rows has one
+// narrow weight-major tile per narrow channel tile instead.
 __device__ __forceinline__ Unit decode_single(int tile, const int32_t* s_off, const int32_t* s_cnt,
-                                              const int32_t* s_start, const GemmArgs& a, bool fc1) {
+                                              const int32_t* s_start, const GemmArgs& a, bool fc1,
+                                              bool narrow_launch) {
   const int g = find_group(tile, s_off, a.G);
   const int m = s_cnt[g];
+  if (narrow_launch && m <= kNarrowRows) {
+    const bool shared = g >= a.E;
+    Unit t;
+    t.g = g;
+    t.K = shared ? a.K_shared : a.K_routed;
+    t.N = shared ? a.N_shared : a.N_routed;
+    t.narrow = 1;
+    t.token_major = 0;
+    t.n0 = (tile - s_off[g]) * (fc1 ? kFc1NarrowCols : kFc2NarrowCols);
+    t.row0 = s_start[g];
+    t.rows = m;
+    t.ntok = (m + 15) & ~15;
+    return t;
+  }
   const int nfull = m / 128;
   const int n_mt = nfull + (m % 128 != 0);
   const int local = tile - s_off[g];
@@ -160,6 +178,7 @@ __device__ __forceinline__ Unit decode_single(int tile, const int32_t* s_off, co
   t.K = shared ? a.K_shared : a.K_routed;
   t.N = shared ? a.N_shared : a.N_routed;
   t.n0 = nt * (fc1 ? kFc1Cols : kFc2Cols);
+  t.narrow = 0;
   t.token_major = mt < nfull;
   t.row0 = s_start[g] + mt * 128;
   t.rows = min(128, m - mt * 128);
@@ -272,35 +291,6 @@ __device__ __forceinline__ void store_weight_major(uint32_t tb, const Unit& t, i
   }
 }
 
-// Single-SM weight-major epilogue: thread = channel lrow (of the 128 in D0, and of D1);
-// TMEM columns = token rows. FC1: D0 gate, D1 up of the same channel; FC2: D0 channels
-// n0..n0+127, D1 channels n0+128..n0+255.
-template <bool kFc1>
-__device__ __forceinline__ void store_weight_major_single(uint32_t tb, const Unit& t, int lrow,
-                                                          const GemmArgs& a) {
-  float va[16], vb[16];
-  const int ch0 = t.n0 + lrow;
-  const int ch1 = kFc1 ? ch0 : (t.n0 + 128 + lrow);
-  const bool v0 = ch0 < t.N, v1 = ch1 < t.N;
-#pragma unroll 1
-  for (int c0 = 0; c0 < t.ntok; c0 += 16) {
-    tmem_ld2_x16(tb + c0, tb + 128 + c0, va, vb);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int r = c0 + i;
-      if (r < t.rows) {
-        __nv_bfloat16* orow = a.out + static_cast<int64_t>(t.row0 + r) * a.out_ld;
-        if (kFc1) {
-          if (v0) orow[ch0] = __float2bfloat16_rn(silu(va[i]) * vb[i]);
-        } else {
-          if (v0) orow[ch0] = __float2bfloat16_rn(va[i]);
-          if (v1) orow[ch1] = __float2bfloat16_rn(vb[i]);
-        }
-      }
-    }
-  }
-}
-
 // Both kernels: the last CTA to finish resets the work counter for the next launch.
 __device__ __forceinline__ void finish_claims(const GemmArgs& a) {
   __threadfence();
@@ -347,15 +337,50 @@ __device__ __forceinline__ bool single_k_loop(uint32_t d, uint32_t idesc, int nk
   return true;
 }
 
-template <bool kFc1>
-__global__ void __launch_bounds__(kThreads, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, box 64 x 128
-                    const __grid_constant__ CUtensorMap map_x16,    // A rows, box 64 x 16
-                    const __grid_constant__ CUtensorMap map_w,      // routed weights [E, R, K]
-                    const __grid_constant__ CUtensorMap map_ws,     // shared weights [1, R, K]
-                    GemmArgs a) {
+// The K loop of a narrow weight-major tile: each stage holds two K blocks (the last one
+// may hold one), each a 128-row W block (FC1: 64 gate rows, then the 64 up rows of the
+// same channels) and the tile's X rows; one MMA per 16 K, A = the W block, B = X (N = ntok).
+__device__ __forceinline__ bool single_k_loop_narrow(uint32_t d, uint32_t idesc, int nkb,
+                                                     int& stage, uint32_t& phase, uint32_t sx0,
+                                                     uint32_t sw0, uint64_t* full_bar,
+                                                     uint64_t* empty_bar, volatile int* abort) {
+  for (int kb = 0; kb < nkb; kb += 2) {
+    if (!mbar_wait(&full_bar[stage], phase, abort)) return false;
+    tc_fence_after();
+    const uint32_t xa = sx0 + stage * kXStageBytes;
+    const uint32_t wa = sw0 + stage * (2 * kWStageBytes);
+    const int nk = nkb - kb < 2 ? 1 : 2;
+    for (int b = 0; b < nk; ++b) {
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        umma_bf16(d, sdesc_k_major(wa + b * kWStageBytes + kk * 32, kRowBytes),
+                  sdesc_k_major(xa + b * (kXStageBytes / 2) + kk * 32, kRowBytes), idesc,
+                  (kb | b | kk) != 0);
+      }
+    }
+    umma_commit(&empty_bar[stage]);
+    if (++stage == kSingleStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+  return true;
+}
+
+// The single-SM kernel. kNarrow: a launch whose small groups get narrow weight-major
+// tiles (see narrow_max_rows); only that form reads the 64-row weight maps. The tensor
+// maps are kernel parameters (__grid_constant__), passed here by address.
+template <bool kFc1, bool kNarrow>
+__device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128,  // A, box 64 x 128
+                                                   const CUtensorMap* map_x16,   // A, box 64 x 16
+                                                   const CUtensorMap* map_w,     // routed [E, R, K]
+                                                   const CUtensorMap* map_ws,    // shared [1, R, K]
+                                                   const CUtensorMap* map_w64,   // routed, 64 rows
+                                                   const CUtensorMap* map_ws64,  // shared, 64 rows
+                                                   const GemmArgs& a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kSingleStages], empty_bar[kSingleStages];
+  __shared__ float s_xchg[kNarrow ? 64 * kXchgStride : 1];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint64_t sched_full[kSchedDepth], sched_empty[kSchedDepth];
   __shared__ int s_tile[kSchedDepth];
@@ -391,10 +416,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_map(&map_x128);
-    tma_prefetch_map(&map_x16);
-    tma_prefetch_map(&map_w);
-    tma_prefetch_map(&map_ws);
+    tma_prefetch_map(map_x128);
+    tma_prefetch_map(map_x16);
+    tma_prefetch_map(map_w);
+    tma_prefetch_map(map_ws);
+    if (kFc1 && kNarrow) {
+      tma_prefetch_map(map_w64);
+      tma_prefetch_map(map_ws64);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&s_tmem_base, kTmemCols);
@@ -433,33 +462,55 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
         s_tile[slot] = tile;
         mbar_arrive(&sched_full[slot]);
         if (tile < 0) break;
-        const Unit t = decode_single(tile, s_off, s_cnt, s_start, a, kFc1);
+        const Unit t = decode_single(tile, s_off, s_cnt, s_start, a, kFc1, kNarrow);
         const bool shared = t.g >= a.E;
-        const CUtensorMap* mw = shared ? &map_ws : &map_w;
+        const CUtensorMap* mw = shared ? map_ws : map_w;
         const int ecoord = shared ? 0 : t.g - a.plane_off;
         const int wr0 = t.n0;
         const int wr1 = kFc1 ? (t.N + t.n0) : (t.n0 + 128);
-        const uint32_t bytes =
-            (2 * kWStageBytes) + (t.token_major ? kXStageBytes : static_cast<uint32_t>(t.ntok) * kRowBytes);
+        const uint32_t xbytes = static_cast<uint32_t>(t.ntok) * kRowBytes;
+        const uint32_t bytes = (2 * kWStageBytes) + (t.token_major ? kXStageBytes : xbytes);
         const int nkb = t.K / kBK;
-        for (int kb = 0; kb < nkb; ++kb) {
+        // Narrow tiles: two K blocks per stage; FC1 W blocks are 64 gate rows (64-row
+        // boxes) then the 64 up rows, FC2 W blocks 128 channel rows.
+        const CUtensorMap* mwn = kFc1 ? (shared ? map_ws64 : map_w64) : mw;
+        const int nst = kNarrow && t.narrow ? (nkb + 1) >> 1 : nkb;
+        for (int j = 0; j < nst; ++j) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort)) {
             flag_timeout(a.status, abort);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_bar[stage], bytes);
-          const int kc = kb * kBK;
           uint8_t* xs = sX + stage * kXStageBytes;
           uint8_t* ws = sW + stage * (2 * kWStageBytes);
-          if (t.token_major) {
-            tma_load_2d(xs, &map_x128, &full_bar[stage], kc, t.row0);
+          if (kNarrow && t.narrow) {
+            const int nk = nkb - 2 * j < 2 ? 1 : 2;
+            mbar_arrive_expect_tx(&full_bar[stage], nk * (kWStageBytes + xbytes));
+            for (int b = 0; b < nk; ++b) {
+              const int kc = (2 * j + b) * kBK;
+              uint8_t* xb = xs + b * (kXStageBytes / 2);
+              uint8_t* wb = ws + b * kWStageBytes;
+              for (int r = 0; r < t.ntok; r += 16)
+                tma_load_2d(xb + r * kRowBytes, map_x16, &full_bar[stage], kc, t.row0 + r);
+              if (kFc1) {
+                tma_load_3d(wb, mwn, &full_bar[stage], kc, t.n0, ecoord);
+                tma_load_3d(wb + kWStageBytes / 2, mwn, &full_bar[stage], kc, t.N + t.n0, ecoord);
+              } else {
+                tma_load_3d(wb, mwn, &full_bar[stage], kc, t.n0, ecoord);
+              }
+            }
           } else {
-            for (int r = 0; r < t.ntok; r += 16)
-              tma_load_2d(xs + r * kRowBytes, &map_x16, &full_bar[stage], kc, t.row0 + r);
+            mbar_arrive_expect_tx(&full_bar[stage], bytes);
+            const int kc = j * kBK;
+            if (t.token_major) {
+              tma_load_2d(xs, map_x128, &full_bar[stage], kc, t.row0);
+            } else {
+              for (int r = 0; r < t.ntok; r += 16)
+                tma_load_2d(xs + r * kRowBytes, map_x16, &full_bar[stage], kc, t.row0 + r);
+            }
+            tma_load_3d(ws, mw, &full_bar[stage], kc, wr0, ecoord);
+            tma_load_3d(ws + kWStageBytes, mw, &full_bar[stage], kc, wr1, ecoord);
           }
-          tma_load_3d(ws, mw, &full_bar[stage], kc, wr0, ecoord);
-          tma_load_3d(ws + kWStageBytes, mw, &full_bar[stage], kc, wr1, ecoord);
           ++issued;
           if (++stage == kSingleStages) {
             stage = 0;
@@ -502,7 +553,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
         const int tile = *reinterpret_cast<volatile int*>(&s_tile[slot]);
         mbar_arrive(&sched_empty[slot]);
         if (tile < 0) break;
-        const Unit t = decode_single(tile, s_off, s_cnt, s_start, a, kFc1);
+        const Unit t = decode_single(tile, s_off, s_cnt, s_start, a, kFc1, kNarrow);
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort)) {
           flag_timeout(a.status, abort);
           ok = false;
@@ -511,10 +562,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
         const int nkb = t.K / kBK;
-        ok = t.token_major ? single_k_loop<true>(d, idesc_bf16_f32(128, 256), nkb, stage, phase,
-                                                 sx0, sw0, full_bar, empty_bar, abort)
-                           : single_k_loop<false>(d, idesc_bf16_f32(128, t.ntok), nkb, stage,
-                                                  phase, sx0, sw0, full_bar, empty_bar, abort);
+        if (kNarrow && t.narrow)
+          ok = single_k_loop_narrow(d, idesc_bf16_f32(128, t.ntok), nkb, stage, phase, sx0, sw0,
+                                    full_bar, empty_bar, abort);
+        else if (t.token_major)
+          ok = single_k_loop<true>(d, idesc_bf16_f32(128, 256), nkb, stage, phase, sx0, sw0,
+                                   full_bar, empty_bar, abort);
+        else
+          ok = single_k_loop<false>(d, idesc_bf16_f32(128, t.ntok), nkb, stage, phase, sx0, sw0,
+                                    full_bar, empty_bar, abort);
         if (!ok) {
           flag_timeout(a.status, abort);
           break;
@@ -549,7 +605,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
       __syncwarp();
       if (lane == 0) mbar_arrive(&sched_empty[slot]);
       if (tile < 0) break;
-      const Unit t = decode_single(tile, s_off, s_cnt, s_start, a, kFc1);
+      const Unit t = decode_single(tile, s_off, s_cnt, s_start, a, kFc1, kNarrow);
       const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort);
       // Lanes may leave the poll at different times; tcgen05.ld is warp-collective.
       if (!__all_sync(0xffffffffu, got)) {
@@ -560,7 +616,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
       const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * kAccCols) +
                           (static_cast<uint32_t>(q * 32) << 16);
       float va[16], vb[16];
-      if (t.token_major) {
+      if (kNarrow && t.narrow) {
+        // Lane = weight row of the narrow tile (FC1: gate lanes 0-63, up lanes 64-127).
+        store_weight_major<kFc1>(tb, t, lrow, 0u, s_xchg, a);
+      } else if (t.token_major) {
         // Thread = token row lrow; columns = channels.
         const bool valid = lrow < t.rows;
         __nv_bfloat16* orow = a.out + static_cast<int64_t>(t.row0 + lrow) * a.out_ld;
@@ -636,6 +695,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128,   // A rows, b
     tmem_dealloc(tmem_base, kTmemCols);
   }
   if (threadIdx.x == 0) finish_claims(a);
+}
+
+template <bool kFc1>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128, const __grid_constant__ CUtensorMap map_x16,
+                    const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_ws,
+                    GemmArgs a) {
+  single_kernel_body<kFc1, false>(&map_x128, &map_x16, &map_w, &map_ws, nullptr, nullptr, a);
+}
+
+template <bool kFc1>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_narrow_kernel(const __grid_constant__ CUtensorMap map_x128,
+                           const __grid_constant__ CUtensorMap map_x16,
+                           const __grid_constant__ CUtensorMap map_w,
+                           const __grid_constant__ CUtensorMap map_ws,
+                           const __grid_constant__ CUtensorMap map_w64,
+                           const __grid_constant__ CUtensorMap map_ws64, GemmArgs a) {
+  single_kernel_body<kFc1, true>(&map_x128, &map_x16, &map_w, &map_ws, &map_w64, &map_ws64, a);
 }
 
 // ============================================================== CTA-pair kernel
@@ -956,6 +1034,9 @@ moe_status prepare_kernels(int* max_clusters) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kFc1>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSingleSmemBytes);
     if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_gemm_narrow_kernel<kFc1>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSingleSmemBytes);
+    if (e == cudaSuccess)
       e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kFc1>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess)
@@ -1038,7 +1119,10 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
   const int64_t n_nt = kFc1 ? (nI + kFc1Cols - 1) / kFc1Cols : (p.H + kFc2Cols - 1) / kFc2Cols;
   const bool use_pairs = pair_min_rows(p) <= 2 * kTileRows;
   const int64_t pair_bound = use_pairs ? (R / 256 + L.groups) * n_nt : 0;
-  const int64_t single_bound = use_pairs ? 0 : (R / kTileRows + L.groups) * n_nt;
+  // (A narrow tile is half a channel tile wide: at most twice as many tiles.)
+  const bool narrow = narrow_max_rows(p) > 0;
+  const int64_t single_bound =
+      use_pairs ? 0 : (narrow ? 2 : 1) * (R / kTileRows + L.groups) * n_nt;
 
   cudaError_t err = cudaSuccess;
   if (single_bound > 0) {
@@ -1048,8 +1132,13 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
     int64_t grid = device_sm_count();
     if (grid > single_bound) grid = single_bound;
     if (grid < 1) grid = 1;
-    err = launch_pdl(grouped_gemm_kernel<kFc1>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
-                     kSingleSmemBytes, s, mx128, mx16, mw128, mws128, as);
+    if (narrow)
+      err = launch_pdl(grouped_gemm_narrow_kernel<kFc1>, dim3(static_cast<unsigned>(grid)),
+                       dim3(kThreads), kSingleSmemBytes, s, mx128, mx16, mw128, mws128, mw64, mws64,
+                       as);
+    else
+      err = launch_pdl(grouped_gemm_kernel<kFc1>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
+                       kSingleSmemBytes, s, mx128, mx16, mw128, mws128, as);
   }
   if (err == cudaSuccess && pair_bound > 0) {
     GemmArgs ap = a;

@@ -88,6 +88,7 @@ struct PlanArgs {
   int shared_I;
   int H;
   int pair_min_rows;   // groups with at least this many rows go to the CTA-pair list
+  int narrow_rows;     // single-SM groups with 1..narrow_rows rows get narrow tiles
   const int32_t* block_hist;
   int32_t* counts;     // [G]
   int32_t* starts;     // [G]
@@ -159,7 +160,9 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
       // Work of the grouped GEMM, per output-channel tile. A group of >= pair_min_rows
       // rows goes to the CTA-pair kernel: floor(m / 256) units of two full 128-row tiles
       // plus one unit for the rows left over. Any other group goes to the single-SM
-      // kernel: one tile per 128 rows (full tiles and/or the partial last one).
+      // kernel: one tile per 128 rows (full tiles and/or the partial last one), or, for a
+      // group of at most narrow_rows rows, one narrow weight-major tile per channel tile
+      // of the narrow width.
       const int nI = (tid < E) ? a.I : a.shared_I;
       const int c1 = (nI + kFc1Cols - 1) / kFc1Cols;
       const int c2 = (a.H + kFc2Cols - 1) / kFc2Cols;
@@ -167,6 +170,9 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
         const int units = (cnt >> 8) + ((cnt & 255) != 0);
         np1 = units * c1;
         np2 = units * c2;
+      } else if (cnt > 0 && cnt <= a.narrow_rows) {
+        ns1 = (nI + kFc1NarrowCols - 1) / kFc1NarrowCols;
+        ns2 = (a.H + kFc2NarrowCols - 1) / kFc2NarrowCols;
       } else {
         const int tiles = cnt / kTileRows + (cnt % kTileRows != 0);
         ns1 = tiles * c1;
@@ -298,6 +304,7 @@ moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const vo
   a.shared_I = p.shared_I;
   a.H = p.H;
   a.pair_min_rows = pair_min_rows(p);
+  a.narrow_rows = narrow_max_rows(p);
   a.block_hist = reinterpret_cast<const int32_t*>(ws + L.block_hist);
   a.counts = reinterpret_cast<int32_t*>(ws + L.counts);
   a.starts = reinterpret_cast<int32_t*>(ws + L.starts);

@@ -127,13 +127,13 @@ def test_route_nonfinite_logits_never_beat_finite(moe):
 # ------------------------------------------------------------------------ permute
 
 @pytest.mark.parametrize("T,E,k", [(300, 8, 2), (5000, 64, 4), (1, 4, 1), (2048, 256, 8), (513, 16, 2),
-                                   (9000, 3, 3)])
+                                   (9000, 3, 3), (1000, 64, 2)])
 def test_permute_parity(moe, T, E, k):
     g = torch.Generator().manual_seed(T + E)
     ids = torch.randint(0, E, (T, k), generator=g, dtype=torch.int32)
-    H = 128
+    H, I = 384, 192
     x = torch.randn(T, H, generator=g).to(torch.bfloat16)
-    p = moe.make_problem(T, H, 64, E, k)
+    p = moe.make_problem(T, H, I, E, k)
     ws = moe.alloc_workspace(p)
     moe.moe_permute(p, x.cuda(), ids.cuda(), ws)
     torch.cuda.synchronize()
@@ -145,15 +145,20 @@ def test_permute_parity(moe, T, E, k):
     assert np.array_equal(ws.region("perm_inv", P, torch.int32).cpu().numpy(), perm_inv)
     xp = ws.region("x_perm", P * H, torch.bfloat16).view(P, H).cpu()
     assert torch.equal(xp, x[torch.from_numpy(perm_src).long() // k])
-    # work lists (one channel tile each here: I = 64, H = 128). When T * k >= 256 * E the
-    # CTA-pair kernel takes every group: floor(m / 256) + (m % 256 > 0) units each.
-    # Otherwise every group has ceil(m / 128) tiles in the single-SM list.
+    # work lists. Channel tiles: FC1 ceil(I / 128) = 2, FC2 ceil(H / 256) = 2; narrow ones
+    # (64 and 128 channels) ceil(I / 64) = 3 and ceil(H / 128) = 3. When T * k >= 256 * E
+    # the CTA-pair kernel takes every group: floor(m / 256) + (m % 256 > 0) units per
+    # channel tile. Otherwise every group goes to the single-SM list: when T * k <= 32 * E,
+    # one narrow tile per narrow channel tile if 1 <= m <= 32; else ceil(m / 128) tiles per
+    # channel tile.
     big = (counts >= 1) & (T * k >= 256 * E)
     pair_units = np.where(big, counts // 256 + (counts % 256 > 0), 0)
-    single_tiles = np.where(big, 0, counts // 128 + (counts % 128 > 0))
-    for name in ("tile_off1", "tile_off2"):
+    row_tiles = counts // 128 + (counts % 128 > 0)
+    narrow = ~big & (T * k <= 32 * E) & (counts >= 1) & (counts <= 32)
+    for name, wide_c, narrow_c in (("tile_off1", 2, 3), ("tile_off2", 2, 3)):
+        single_tiles = np.where(big, 0, np.where(narrow, narrow_c, row_tiles * wide_c))
         lst = ws.region(name, 2 * (E + 1), torch.int32).cpu().numpy()
-        assert np.array_equal(lst[:E + 1], np.concatenate([[0], np.cumsum(pair_units)]))
+        assert np.array_equal(lst[:E + 1], np.concatenate([[0], np.cumsum(pair_units * wide_c)]))
         assert np.array_equal(lst[E + 1:], np.concatenate([[0], np.cumsum(single_tiles)]))
     st, flags = moe.moe_read_device_status(ws)
     assert st == moe.MOE_OK and flags == 0
@@ -219,6 +224,8 @@ SMALL_CASES = [
     (1, 128, 128, 8, 2, 0, "route"),           # a single token
     (64, 256, 128, 32, 4, 192, "route"),       # shared expert wider than the routed ones
     (96, 128, 256, 8, 2, 64, "route"),         # shared expert narrower than the routed ones
+    (48, 192, 320, 16, 4, 0, "route"),         # narrow tiles: odd K blocks, ragged FC2 tile
+    (24, 192, 128, 16, 2, 192, "route"),       # narrow shared expert (odd FC2 K blocks)
 ]
 
 
