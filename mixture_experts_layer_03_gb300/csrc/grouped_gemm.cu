@@ -73,6 +73,7 @@ constexpr uint16_t kPairMask = 0x3;
 // epilogue warps, and the second CTA's producer and 4 epilogue warps.
 constexpr uint32_t kSchedConsumers = 1 + 4 + 1 + 4;
 constexpr int kXchgStride = 17;                      // padded row of the gate/up swap buffer
+constexpr int64_t kPrefetchBytes = 48ll << 20;       // narrow FC1 L2 prefetch, whole grid
 
 struct GemmArgs {
   const int32_t* counts;    // [G]
@@ -87,6 +88,9 @@ struct GemmArgs {
   int64_t out_ld;
   int32_t* status;
   int32_t* sched;           // [0] next unit to claim, [1] CTAs finished (both reset at exit)
+  int32_t planes;           // routed weight planes in the maps (experts of this call)
+  int32_t prefetch_kb;      // narrow FC1: K blocks of its guessed first tile each CTA
+                            // prefetches into L2 before the work lists exist (0: none)
 };
 
 struct Unit {
@@ -423,6 +427,25 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
     if (kFc1 && kNarrow) {
       tma_prefetch_map(map_w64);
       tma_prefetch_map(map_ws64);
+      // The kernels before this one (routing and the permutation) leave HBM idle. Pull
+      // this CTA's likely first tiles into L2 meanwhile: the claims of round r are list
+      // entries r * gridDim.x .. (r + 1) * gridDim.x - 1, and with every expert active
+      // entry b is expert b / tiles-per-expert, narrow tile b mod tiles-per-expert. A
+      // wrong guess (an inactive expert) only costs idle bandwidth.
+      const int tpe = (a.N_routed + kFc1NarrowCols - 1) / kFc1NarrowCols;
+      const int nkb = a.K_routed / kBK;
+      int left = a.prefetch_kb;
+      for (int b = static_cast<int>(blockIdx.x); left > 0; b += static_cast<int>(gridDim.x)) {
+        const int g = b / tpe;
+        if (g >= a.planes) break;
+        const int n0 = (b - g * tpe) * kFc1NarrowCols;
+        const int n = left < nkb ? left : nkb;
+        for (int kb = 0; kb < n; ++kb) {
+          tma_prefetch_3d(map_w64, kb * kBK, n0, g);
+          tma_prefetch_3d(map_w64, kb * kBK, a.N_routed + n0, g);
+        }
+        left -= n;
+      }
     }
   }
   if (warp == 1) {
@@ -1108,6 +1131,8 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
     a.out_ld = p.H;
   }
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
+  a.planes = e_hi - e_lo;
+  a.prefetch_kb = 0;
   // Work lists [pair units | single-SM tiles], each G+1 offsets; counters [pair | single].
   const int32_t* lists = reinterpret_cast<const int32_t*>(ws + (kFc1 ? L.tile_off1 : L.tile_off2));
   int32_t* sched = reinterpret_cast<int32_t*>(ws + L.sched) + (kFc1 ? 0 : 4);
@@ -1132,6 +1157,13 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
     int64_t grid = device_sm_count();
     if (grid > single_bound) grid = single_bound;
     if (grid < 1) grid = 1;
+    if (kFc1 && narrow) {
+      // L2 prefetch of each CTA's guessed first tiles (see the kernel), kPrefetchBytes
+      // over the grid: two 64-row boxes (16 KB) per K block.
+      const int64_t per_kb = 2 * 64 * kRowBytes;
+      const int64_t kb = kPrefetchBytes / (grid * per_kb);
+      as.prefetch_kb = static_cast<int32_t>(kb < (1 << 20) ? kb : (1 << 20));
+    }
     if (narrow)
       err = launch_pdl(grouped_gemm_narrow_kernel<kFc1>, dim3(static_cast<unsigned>(grid)),
                        dim3(kThreads), kSingleSmemBytes, s, mx128, mx16, mw128, mws128, mw64, mws64,
