@@ -266,6 +266,18 @@ moe_status moe_finalize(const moe_problem* p, const float* scales, void* y, void
  * MOE_ERR_DEVICE_TIMEOUT when a bit is set, else MOE_OK. */
 moe_status moe_read_device_status(void* workspace, void* stream, int32_t* flags);
 
+/* Self-test of the device failure path, with no fault and no hang: one kernel (one CTA)
+ * whose two pipeline roles wait on mbarriers that nothing arrives on, with the same
+ * bounded wait as every pipelined kernel here (2 s of wall clock). The producer's wait
+ * runs out, sets MOE_DEVICE_FLAG_TIMEOUT in the workspace status word and raises the
+ * abort flag; the consumer, which started waiting 1 s later, leaves through that flag
+ * and sets status word 1 to 1 when it left before its own limit. `workspace`: any
+ * workspace of this library (16-byte aligned; only its first 16 bytes are touched, and
+ * words 0-1 are cleared first). Enqueued on `stream`; returns at once. The timeout then
+ * reads back through moe_read_device_status, and the context stays usable. Errors:
+ * MOE_ERR_INVALID_ARG (NULL or misaligned workspace), MOE_ERR_CUDA (launch). */
+moe_status moe_selftest_wait(void* workspace, void* stream);
+
 /* Round-to-nearest-even conversion of n fp32 values to bf16 (device in/out). */
 moe_status moe_cast_f32_to_bf16(const float* in, void* out, int64_t n, void* stream);
 

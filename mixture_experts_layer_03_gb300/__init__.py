@@ -79,6 +79,7 @@ _SIGS = {
     "moe_fc2": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_finalize": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_read_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
+    "moe_selftest_wait": (ctypes.c_int, [_P, _P]),
     "moe_cast_f32_to_bf16": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P]),
 }
 EXPORTED = tuple(_SIGS)
@@ -328,6 +329,12 @@ def moe_read_device_status(workspace: Workspace, stream=None):
     flags = ctypes.c_int32(0)
     st = _lib.moe_read_device_status(workspace.ptr, _stream(stream), ctypes.byref(flags))
     return st, flags.value
+
+
+def moe_selftest_wait(workspace: Workspace, stream=None):
+    """Enqueue the device failure-path self-test on ``workspace``'s status words: a
+    bounded wait that runs out after about 2 s and reports MOE_DEVICE_FLAG_TIMEOUT."""
+    _check(_lib.moe_selftest_wait(workspace.ptr, _stream(stream)), "moe_selftest_wait")
 
 
 def moe_cast_f32_to_bf16(t: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None):

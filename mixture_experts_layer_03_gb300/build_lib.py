@@ -21,7 +21,8 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build", platform.machine())
 LIB_NAME = "libmoe_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
-SOURCES = ["api.cu", "route.cu", "permute.cu", "grouped_gemm.cu", "finalize.cu", "gate.cu"]
+SOURCES = ["api.cu", "route.cu", "permute.cu", "grouped_gemm.cu", "finalize.cu", "gate.cu",
+           "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

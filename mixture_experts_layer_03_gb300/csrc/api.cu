@@ -370,6 +370,15 @@ moe_status moe_read_device_status(void* workspace, void* stream, int32_t* flags)
   return MOE_OK;
 }
 
+moe_status moe_selftest_wait(void* workspace, void* stream) {
+  if (!workspace) return set_error(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  if (!aligned16(workspace)) return set_error(MOE_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, 2 * sizeof(int32_t), s);
+  if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
+  return launch_wait_selftest(static_cast<int32_t*>(workspace), s);
+}
+
 moe_status moe_cast_f32_to_bf16(const float* in, void* out, int64_t n, void* stream) {
   if (n < 0) return set_error(MOE_ERR_INVALID_ARG, "negative length");
   if (n == 0) return MOE_OK;

@@ -76,6 +76,9 @@ moe_status launch_fc2(const moe_problem& p, const moe_ws_layout& L, const void* 
 moe_status launch_finalize(const moe_problem& p, const moe_ws_layout& L, const float* scales,
                            const float* shared_gate, void* y, const char* ws, cudaStream_t s);
 
+// Device failure-path self-test (selftest.cu): status = the workspace status words.
+moe_status launch_wait_selftest(int32_t* status, cudaStream_t s);
+
 moe_status launch_gate(const void* x, const void* wg, int64_t T, int H, int E, int n_shared,
                        float* logits, float* shared_logits, int32_t* status, cudaStream_t s);
 

@@ -148,3 +148,6 @@ def test_forward_host_errors(moe):
     assert lib.moe_cast_f32_to_bf16(None, None, -1, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_cast_f32_to_bf16(None, None, 0, None) == moe.MOE_OK
     assert lib.moe_read_device_status(None, None, None) == moe.MOE_ERR_INVALID_ARG
+    # the failure-path self-test checks its workspace pointer on the host
+    assert lib.moe_selftest_wait(None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_wait(ctypes.c_void_p(8), None) == moe.MOE_ERR_INVALID_ARG

@@ -396,6 +396,36 @@ def test_bad_ids_are_skipped_and_flagged(moe):
     assert pinv[3 * 2 + 1] == -1 and pinv[10 * 2 + 0] == -1
 
 
+def test_device_wait_timeout_is_reported_and_the_context_stays_usable(moe):
+    """The failure path without a fault: a pipeline wait that nothing completes runs out
+    after the kernels' 2 s limit, the host reads MOE_DEVICE_FLAG_TIMEOUT, the other role
+    (which would have waited until 3 s) is released by the abort flag, and a forward on
+    the same context afterwards is correct and reports no error."""
+    import time
+    c = _random_case(64, 128, 128, 8, 2, 0, seed=7)
+    p, ws, y0, dev = _run_forward_steps(moe, c)
+    assert moe.moe_read_device_status(ws)[0] == moe.MOE_OK
+    t0 = time.perf_counter()
+    moe.moe_selftest_wait(ws)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    released = int(ws.region("status", 4, torch.int32)[1].item())
+    st, flags = moe.moe_read_device_status(ws)
+    assert st == moe.MOE_ERR_DEVICE_TIMEOUT and flags & moe.MOE_DEVICE_FLAG_TIMEOUT
+    assert released == 1, "the consumer waited out its own limit: the abort flag did not reach it"
+    assert 1.5 < dt < 2.8, dt
+    y = torch.empty_like(y0)
+    moe.moe_permute(p, dev["x"], dev["ids"], ws)
+    moe.moe_fc1(p, dev["w13"], None, ws)
+    moe.moe_fc2(p, dev["w2"], None, ws)
+    moe.moe_finalize(p, dev["sc"], y, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws)[0] == moe.MOE_OK
+    assert torch.equal(y, y0)
+    y_ref = oracle.forward(_np64(c["x"]), c["ids"], c["sc"], _np64(c["w13"]), _np64(c["w2"]))
+    _check_close(y.cpu().double().numpy(), y_ref, Y_TOL, "y after the self-test")
+
+
 def test_zero_tokens_is_a_noop(moe):
     x = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
     ids = torch.empty(0, 2, dtype=torch.int32, device="cuda")
