@@ -1,5 +1,6 @@
 // C ABI entry points: argument validation on the host, workspace layout, and the
 // launch sequence of the forward. Nothing here allocates device memory.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -57,7 +58,8 @@ int32_t route_reason(int64_t T, const moe_route_params& r) {
   }
 }
 
-int g_sm_count[64] = {0};
+// Per-device SM counts, filled on first use (any thread may fill one; all write the same).
+std::atomic<int> g_sm_count[64];
 
 }  // namespace
 
@@ -72,12 +74,12 @@ moe_status set_error(moe_status s, const char* fmt, ...) {
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (g_sm_count[dev] == 0) {
-    int n = 0;
+  int n = g_sm_count[dev].load(std::memory_order_acquire);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
-    g_sm_count[dev] = n;
+    g_sm_count[dev].store(n, std::memory_order_release);
   }
-  return g_sm_count[dev];
+  return n;
 }
 
 bool compute_layout(const moe_problem& p, moe_ws_layout* out) {

@@ -10,6 +10,7 @@
 // (read through distributed shared memory) in rank order, so the sums are deterministic.
 // Rows past T and columns past E + n_shared are zero-filled by the tensor maps and not
 // stored.
+#include <atomic>
 #include <cstdint>
 
 #include <cuda.h>
@@ -206,14 +207,16 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
 
 moe_status launch_gate(const void* x, const void* wg, int64_t T, int H, int E, int n_shared,
                        float* logits, float* shared_logits, int32_t* status, cudaStream_t s) {
-  static bool attr_done[64] = {false};
+  // The shared-memory opt-in, once per device (published after it is set; a thread that
+  // finds it unset sets it again, which is harmless).
+  static std::atomic<bool> attr_done[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
+  if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_acquire)) {
     const cudaError_t e =
         cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGateSmemBytes);
     if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "gate smem attribute: %s", cudaGetErrorString(e));
-    attr_done[dev] = true;
+    if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
   }
   GateArgs g;
   g.T = T;

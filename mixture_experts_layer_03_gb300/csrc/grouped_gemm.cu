@@ -40,6 +40,7 @@
 //
 // Rows past a group's end inside a tile read the next group's rows (or zero fill past
 // the tensor); they only reach accumulator rows/columns that the epilogue masks.
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 
@@ -1045,15 +1046,18 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
 // ---------------------------------------------------------------- host side
 
 
-// Per device: the large dynamic shared memory opt-in of both kernels, and how many 2-CTA
-// clusters of the pair kernel can be resident at once.
+// Per device: the large dynamic shared memory opt-in of the kernels, and how many 2-CTA
+// clusters of the pair kernel can be resident at once. The count is published (release)
+// only after the attributes are set, so a thread that reads it (acquire) may launch; two
+// threads that both find it unset both do the same idempotent work.
 template <bool kFc1>
 moe_status prepare_kernels(int* max_clusters) {
-  static int clusters_dev[64] = {0};
+  static std::atomic<int> clusters_dev[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
     return set_error(MOE_ERR_CUDA, "cudaGetDevice failed");
-  if (!clusters_dev[dev]) {
+  int have = clusters_dev[dev].load(std::memory_order_acquire);
+  if (!have) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kFc1>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSingleSmemBytes);
     if (e == cudaSuccess)
@@ -1075,9 +1079,10 @@ moe_status prepare_kernels(int* max_clusters) {
       cudaGetLastError();   // clear the failed query; fall back to one cluster per SM pair
       n = sms / 2;
     }
-    clusters_dev[dev] = n;
+    clusters_dev[dev].store(n, std::memory_order_release);
+    have = n;
   }
-  *max_clusters = clusters_dev[dev];
+  *max_clusters = have;
   return MOE_OK;
 }
 

@@ -426,6 +426,66 @@ def test_device_wait_timeout_is_reported_and_the_context_stays_usable(moe):
     _check_close(y.cpu().double().numpy(), y_ref, Y_TOL, "y after the self-test")
 
 
+_THREADED_SCRIPT = r"""
+import sys, threading, torch
+import mixture_experts_layer_03_gb300 as moe
+shapes = [  # T, H, I, E, k, shared_I: single-SM, narrow, CTA-pair, shared-expert launches
+    (300, 256, 192, 8, 2, 0), (48, 192, 320, 16, 4, 0), (2200, 256, 192, 4, 2, 256),
+    (64, 256, 128, 32, 4, 192), (513, 128, 128, 8, 8, 0), (1, 128, 128, 8, 2, 0)]
+g = torch.Generator().manual_seed(3)
+cases = []
+for T, H, I, E, k, sI in shapes:
+    c = dict(x=torch.randn(T, H, generator=g).to(torch.bfloat16),
+             ids=torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).int(),
+             sc=torch.rand(T, k, generator=g),
+             w13=(torch.randn(E, 2 * I, H, generator=g) * H ** -0.5).to(torch.bfloat16),
+             w2=(torch.randn(E, H, I, generator=g) * I ** -0.5).to(torch.bfloat16),
+             w13s=(torch.randn(2 * sI, H, generator=g) * H ** -0.5).to(torch.bfloat16) if sI else None,
+             w2s=(torch.randn(H, sI, generator=g) * sI ** -0.5).to(torch.bfloat16) if sI else None)
+    cases.append({n: (None if v is None else v.cuda()) for n, v in c.items()})
+torch.cuda.synchronize()
+
+def run(c, stream=None):
+    return moe.moe_forward(c["x"], c["ids"], c["sc"], c["w13"], c["w2"], c["w13s"], c["w2s"],
+                           stream=stream)
+
+out, err = [None] * len(cases), []
+start = threading.Barrier(len(cases))
+def worker(i):
+    try:
+        s = torch.cuda.Stream()
+        start.wait()                      # every thread's first call at the same moment
+        with torch.cuda.stream(s):
+            y = run(cases[i], s)
+        s.synchronize()
+        out[i] = y
+    except Exception as e:
+        err.append(repr(e))
+ts = [threading.Thread(target=worker, args=(i,)) for i in range(len(cases))]
+for t in ts: t.start()
+for t in ts: t.join()
+assert not err, err
+for i, c in enumerate(cases):
+    y = run(c)
+    torch.cuda.synchronize()
+    assert torch.equal(y, out[i]), f"case {i}: threaded result differs"
+print("threaded-ok")
+"""
+
+
+def test_concurrent_calls_from_host_threads_in_a_fresh_process():
+    """The library's one-time per-device setup and its launches from several host threads
+    at once (each thread: its own stream and workspace, first use in a fresh process)
+    give the same bytes as the same forwards run one after another."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _THREADED_SCRIPT], cwd=root, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0 and "threaded-ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
+
+
 def test_zero_tokens_is_a_noop(moe):
     x = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
     ids = torch.empty(0, 2, dtype=torch.int32, device="cuda")
