@@ -139,13 +139,20 @@ def host_inputs(inp: dict) -> dict:
     return out
 
 
-def cpu_baseline(w: Workload, inp_host: dict, target_s: float = 10.0):
-    """The oracle on a sample sized for ~target_s of CPU work (cost = a + b * tokens)."""
+def oracle_sample_tokens(w: Workload, inp_host: dict, target_s: float) -> int:
+    """Tokens of w the oracle processes in about target_s on this host. The oracle's cost
+    is a + b * tokens (a: reading every active expert's weights in fp64; b: the per-token
+    work), fitted from an 8- and a 32-token run; at least 32 tokens, at most the batch."""
     _, t1, n1 = oracle_tokens_per_s(w, inp_host, 8)
     _, t2, n2 = oracle_tokens_per_s(w, inp_host, 32)
     b = max((t2 - t1) / max(n2 - n1, 1), 1e-6)
     a = max(t1 - b * n1, 0.0)
-    n = int(min(w.T, max(32, (target_s - a) / b)))
+    return int(min(w.T, max(32, (target_s - a) / b)))
+
+
+def cpu_baseline(w: Workload, inp_host: dict, target_s: float = 10.0):
+    """The oracle on a sample sized for ~target_s of CPU work."""
+    n = oracle_sample_tokens(w, inp_host, target_s)
     rate, dt, n = oracle_tokens_per_s(w, inp_host, n)
     cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
     return {"value": round(rate, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -432,8 +439,7 @@ def run_reference(args):
     w = WORKLOADS[args.workload]
     inp = make_inputs(w, device="cpu", seed=0)
     inp_host = host_inputs(inp)
-    rate0, dt0, _ = oracle_tokens_per_s(w, inp_host, 8)
-    per_step = int(min(w.T, max(8, 8 * 4.0 / max(dt0, 1e-3))))   # ~4 s per step
+    per_step = oracle_sample_tokens(w, inp_host, 7.0)   # ~7 s per step
     for _ in range(args.warmup):
         oracle_tokens_per_s(w, inp_host, per_step)
     total_t, total_n = 0.0, 0
