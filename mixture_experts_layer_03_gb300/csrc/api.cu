@@ -292,11 +292,11 @@ moe_status moe_forward(const moe_problem* p, const void* x, const int32_t* ids, 
 
 }  // extern "C"
 
-namespace {
-
 // Scratch of moe_forward_static: one fixed array per GPU, in this library's device
 // image. The extra 1024 bytes let the workspace start on a 1024-byte boundary.
-__device__ __align__(256) unsigned char g_static_scratch[MOE_STATIC_SCRATCH_BYTES + 1024];
+static __device__ __align__(256) unsigned char g_static_scratch[MOE_STATIC_SCRATCH_BYTES + 1024];
+
+namespace {
 
 std::mutex g_static_mu;
 void* g_static_addr[64] = {nullptr};
