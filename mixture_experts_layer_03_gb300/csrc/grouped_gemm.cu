@@ -67,8 +67,14 @@ constexpr int kTmemCols = 512;
 constexpr int kThreads = 192;
 constexpr int kMaxGroups = 257;
 constexpr int kSchedDepth = 4;                       // work indices in flight inside a CTA
-constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * (kXStageBytes + kWStageBytes);
-constexpr int kSingleSmemBytes = 1024 + kSingleStages * (kXStageBytes + 2 * kWStageBytes);
+// Epilogue staging of both kernels: per epilogue warp two 32 x 32 bf16 boxes for TMA
+// stores, after the stage ring.
+constexpr int kStoreBufBytes = static_cast<int>(kStoreBoxRows * kStoreBoxCols * 2);
+constexpr int kStageAreaBytes = 4 * 2 * kStoreBufBytes;
+constexpr int kSmemBytes =
+    1024 /*alignment slack*/ + kStages * (kXStageBytes + kWStageBytes) + kStageAreaBytes;
+constexpr int kSingleSmemBytes =
+    1024 + kSingleStages * (kXStageBytes + 2 * kWStageBytes) + kStageAreaBytes;
 constexpr uint16_t kPairMask = 0x3;
 // Consumers that return a scheduling slot to the first CTA: its MMA thread and 4
 // epilogue warps, and the second CTA's producer and 4 epilogue warps.
@@ -246,6 +252,65 @@ __device__ __forceinline__ void store_token_major(uint32_t tb, const Unit& t, in
   }
 }
 
+// Token-major epilogue of a full 128-row tile through shared memory: each epilogue warp
+// converts its 32 rows, 32 columns at a time, into one of its two staging boxes (the
+// store map's 64-byte swizzle) and its lane 0 writes the 32 x 32 box with one TMA store.
+// Stored row by row from registers instead, each store instruction touches 32 rows; at
+// short K those instructions keep the SM's load/store pipe busy for much of the next
+// tile's mainloop and slow the producer's and MMA issuer's shared-memory traffic.
+template <bool kFc1>
+__device__ __forceinline__ void store_token_major_tma(uint32_t tb, const Unit& t, int q, int lane,
+                                                      uint8_t* stage, int& sbuf,
+                                                      const CUtensorMap* map_out) {
+  const int sw = (lane >> 1) & 3;
+  constexpr int kCols = kFc1 ? kFc1Cols : kFc2Cols;
+#pragma unroll 1
+  for (int c0 = 0; c0 < kCols; c0 += static_cast<int>(kStoreBoxCols)) {
+    if (t.n0 + c0 >= t.N) break;   // N is a multiple of 64: whole boxes only
+    uint4 v[4];
+    if (kFc1) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float va[16], vb[16];
+        tmem_ld2_x16(tb + c0 + 16 * h, tb + 128 + c0 + 16 * h, va, vb);
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          pk[i] = pack_bf16x2(silu(va[2 * i]) * vb[2 * i], silu(va[2 * i + 1]) * vb[2 * i + 1]);
+        v[2 * h] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        v[2 * h + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+    } else {
+      float va[16], vb[16];
+      tmem_ld2_x16(tb + c0, tb + c0 + 16, va, vb);
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        pk[i] = pack_bf16x2(va[2 * i], va[2 * i + 1]);
+        pk[8 + i] = pack_bf16x2(vb[2 * i], vb[2 * i + 1]);
+      }
+      v[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      v[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      v[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+      v[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+    }
+    uint8_t* buf = stage + sbuf * kStoreBufBytes;
+    // The box stored from this buffer two boxes ago must have been read out of it.
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+    uint4* row = reinterpret_cast<uint4*>(buf + lane * 64);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) row[j ^ sw] = v[j];
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(map_out, buf, t.n0 + c0, t.row0 + 32 * q);
+      bulk_commit_group();
+    }
+    sbuf ^= 1;
+  }
+}
+
 // Weight-major epilogue: TMEM lane = one of this CTA's 128 weight rows, columns = tokens.
 // FC2: lane L is output channel n0 + 128 * rank + L. FC1: lanes 0-63 are the gate and
 // lanes 64-127 the up projection of channels n0 + 64 * rank + (L mod 64); the up half
@@ -382,6 +447,7 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
                                                    const CUtensorMap* map_ws,    // shared [1, R, K]
                                                    const CUtensorMap* map_w64,   // routed, 64 rows
                                                    const CUtensorMap* map_ws64,  // shared, 64 rows
+                                                   const CUtensorMap* map_out,   // output, 32 x 32
                                                    const GemmArgs& a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kSingleStages], empty_bar[kSingleStages];
@@ -401,6 +467,7 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint8_t* sX = smem;                                   // kSingleStages x 16 KB
   uint8_t* sW = smem + kSingleStages * kXStageBytes;          // kSingleStages x 256 W rows
+  uint8_t* sOut = sW + kSingleStages * 2 * kWStageBytes;      // epilogue staging boxes
 
   pdl_trigger();
   if (threadIdx.x == 0) {
@@ -425,6 +492,7 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
     tma_prefetch_map(map_x16);
     tma_prefetch_map(map_w);
     tma_prefetch_map(map_ws);
+    tma_prefetch_map(map_out);
     if (kFc1 && kNarrow) {
       tma_prefetch_map(map_w64);
       tma_prefetch_map(map_ws64);
@@ -616,6 +684,8 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int lrow = q * 32 + lane;         // accumulator row (lane) of this thread
+    uint8_t* my_out = sOut + q * 2 * kStoreBufBytes;
+    int sbuf = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int it = 0;; ++it) {
@@ -644,42 +714,8 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
         // Lane = weight row of the narrow tile (FC1: gate lanes 0-63, up lanes 64-127).
         store_weight_major<kFc1>(tb, t, lrow, 0u, s_xchg, a);
       } else if (t.token_major) {
-        // Thread = token row lrow; columns = channels.
-        const bool valid = lrow < t.rows;
-        __nv_bfloat16* orow = a.out + static_cast<int64_t>(t.row0 + lrow) * a.out_ld;
-        if (kFc1) {
-#pragma unroll 1
-          for (int c0 = 0; c0 < 128; c0 += 16) {
-            tmem_ld2_x16(tb + c0, tb + 128 + c0, va, vb);
-            if (valid && t.n0 + c0 < t.N) {
-              uint32_t pk[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                pk[i] = pack_bf16x2(silu(va[2 * i]) * vb[2 * i], silu(va[2 * i + 1]) * vb[2 * i + 1]);
-              uint4* dst = reinterpret_cast<uint4*>(orow + t.n0 + c0);
-              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            }
-          }
-        } else {
-#pragma unroll 1
-          for (int c0 = 0; c0 < 256; c0 += 32) {
-            tmem_ld2_x16(tb + c0, tb + c0 + 16, va, vb);
-            if (valid && t.n0 + c0 < t.N) {
-              uint32_t pk[16];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                pk[i] = pack_bf16x2(va[2 * i], va[2 * i + 1]);
-                pk[8 + i] = pack_bf16x2(vb[2 * i], vb[2 * i + 1]);
-              }
-              uint4* dst = reinterpret_cast<uint4*>(orow + t.n0 + c0);
-              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-              dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-              dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
-            }
-          }
-        }
+        // Thread = token row lrow; columns = channels (a full 128-row tile).
+        store_token_major_tma<kFc1>(tb, t, q, lane, my_out, sbuf, map_out);
       } else {
         // Thread = channel lrow (of the 128 in D0, and of D1); columns = tokens.
         const int ch0 = t.n0 + lrow;
@@ -710,6 +746,8 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
         acc_phase ^= 1u;
       }
     }
+    // Every TMA store of this warp has written its box before the CTA ends.
+    if (lane == 0) bulk_wait_group<0>();
   }
 
   __syncthreads();
@@ -725,8 +763,9 @@ template <bool kFc1>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128, const __grid_constant__ CUtensorMap map_x16,
                     const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_ws,
-                    GemmArgs a) {
-  single_kernel_body<kFc1, false>(&map_x128, &map_x16, &map_w, &map_ws, nullptr, nullptr, a);
+                    const __grid_constant__ CUtensorMap map_out, GemmArgs a) {
+  single_kernel_body<kFc1, false>(&map_x128, &map_x16, &map_w, &map_ws, nullptr, nullptr, &map_out,
+                                  a);
 }
 
 template <bool kFc1>
@@ -736,8 +775,10 @@ grouped_gemm_narrow_kernel(const __grid_constant__ CUtensorMap map_x128,
                            const __grid_constant__ CUtensorMap map_w,
                            const __grid_constant__ CUtensorMap map_ws,
                            const __grid_constant__ CUtensorMap map_w64,
-                           const __grid_constant__ CUtensorMap map_ws64, GemmArgs a) {
-  single_kernel_body<kFc1, true>(&map_x128, &map_x16, &map_w, &map_ws, &map_w64, &map_ws64, a);
+                           const __grid_constant__ CUtensorMap map_ws64,
+                           const __grid_constant__ CUtensorMap map_out, GemmArgs a) {
+  single_kernel_body<kFc1, true>(&map_x128, &map_x16, &map_w, &map_ws, &map_w64, &map_ws64,
+                                 &map_out, a);
 }
 
 // ============================================================== CTA-pair kernel
@@ -780,6 +821,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
                     const __grid_constant__ CUtensorMap map_ws128, // shared weights, box 64 x 128
                     const __grid_constant__ CUtensorMap map_w64,   // routed weights, box 64 x 64
                     const __grid_constant__ CUtensorMap map_ws64,  // shared weights, box 64 x 64
+                    const __grid_constant__ CUtensorMap map_out,   // output rows, store box 32 x 32
                     GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
@@ -804,6 +846,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   uint8_t* sX = smem;                                   // kStages x up to 128 X rows
   uint8_t* sW = smem + kStages * kXStageBytes;          // kStages x 128 W rows
+  uint8_t* sOut = sW + kStages * kWStageBytes;          // epilogue staging boxes
 
   pdl_trigger();
   if (threadIdx.x == 0) {
@@ -830,6 +873,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
     tma_prefetch_map(&map_ws128);
     tma_prefetch_map(&map_w64);
     tma_prefetch_map(&map_ws64);
+    tma_prefetch_map(&map_out);
   }
   if (warp == 1) {
     tmem_alloc_pair(&s_tmem_base, kTmemCols);   // collective with the other CTA's warp 1
@@ -994,6 +1038,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
     // -------------------------------------------------------------- epilogue (both CTAs)
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int lrow = q * 32 + lane;         // accumulator row (lane) of this thread
+    uint8_t* my_out = sOut + q * 2 * kStoreBufBytes;
+    int sbuf = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int it = 0;; ++it) {
@@ -1017,8 +1063,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
       tc_fence_after();
       const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * kAccCols) +
                           (static_cast<uint32_t>(q * 32) << 16);
-      if (t.token_major) store_token_major<kFc1>(tb, t, lrow, a);
-      else store_weight_major<kFc1>(tb, t, lrow, rank, s_xchg, a);
+      if (t.token_major && t.rows == kTileRows)
+        store_token_major_tma<kFc1>(tb, t, q, lane, my_out, sbuf, &map_out);
+      else if (t.token_major)
+        store_token_major<kFc1>(tb, t, lrow, a);
+      else
+        store_weight_major<kFc1>(tb, t, lrow, rank, s_xchg, a);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -1030,6 +1080,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
         acc_phase ^= 1u;
       }
     }
+    // Every TMA store of this warp has written its box before the CTA ends.
+    if (lane == 0) bulk_wait_group<0>();
   }
 
   __syncthreads();
@@ -1094,7 +1146,7 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
   if (st != MOE_OK) return st;
   const int64_t R = L.rows;
   const int has_shared = p.shared_I > 0;
-  CUtensorMap mx128, mx8, mx16, mw128, mws128, mw64, mws64;
+  CUtensorMap mx128, mx8, mx16, mw128, mws128, mw64, mws64, mout;
   const void* A = kFc1 ? static_cast<const void*>(ws + L.x_perm) : static_cast<const void*>(ws + L.h);
   const uint64_t a_cols = kFc1 ? static_cast<uint64_t>(p.H) : static_cast<uint64_t>(L.h_ld);
   bool ok = encode_map2(&mx128, A, R, a_cols, 128) && encode_map2(&mx8, A, R, a_cols, 8) &&
@@ -1112,6 +1164,9 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
     ok = ok && encode_map3(&mws128, w_s, 1, sr, sk, 128) && encode_map3(&mws64, w_s, 1, sr, sk, 64);
   else
     ok = ok && encode_map3(&mws128, w, planes, wr, wk, 128) && encode_map3(&mws64, w, planes, wr, wk, 64);
+  // Output rows: FC1 h [R, h_ld], FC2 out_perm [R, H].
+  const uint64_t out_cols = kFc1 ? static_cast<uint64_t>(L.h_ld) : static_cast<uint64_t>(p.H);
+  ok = ok && encode_store_map2(&mout, ws + (kFc1 ? L.h : L.out_perm), R, out_cols);
   if (!ok) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
   GemmArgs a;
@@ -1172,10 +1227,10 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
     if (narrow)
       err = launch_pdl(grouped_gemm_narrow_kernel<kFc1>, dim3(static_cast<unsigned>(grid)),
                        dim3(kThreads), kSingleSmemBytes, s, mx128, mx16, mw128, mws128, mw64, mws64,
-                       as);
+                       mout, as);
     else
       err = launch_pdl(grouped_gemm_kernel<kFc1>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
-                       kSingleSmemBytes, s, mx128, mx16, mw128, mws128, as);
+                       kSingleSmemBytes, s, mx128, mx16, mw128, mws128, mout, as);
   }
   if (err == cudaSuccess && pair_bound > 0) {
     GemmArgs ap = a;
@@ -1184,7 +1239,8 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
     int64_t clusters = max_clusters;
     if (clusters > pair_bound) clusters = pair_bound;
     err = launch_pdl(grouped_gemm_pair_kernel<kFc1>, dim3(static_cast<unsigned>(2 * clusters)),
-                     dim3(kThreads), kSmemBytes, s, mx128, mx8, mw128, mws128, mw64, mws64, ap);
+                     dim3(kThreads), kSmemBytes, s, mx128, mx8, mw128, mws128, mw64, mws64, mout,
+                     ap);
   }
   if (err != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "grouped_gemm launch: %s", cudaGetErrorString(err));

@@ -1,6 +1,7 @@
-// Tensor maps (TMA descriptors) for bf16 operands, shared by the GEMM kernels. Every map
-// moves boxes 64 elements (128 bytes, the swizzle width) wide with the 128-byte swizzle
-// that the UMMA shared-memory descriptors expect. Host code.
+// Tensor maps (TMA descriptors) for bf16 operands, shared by the GEMM kernels. Every load
+// map moves boxes 64 elements (128 bytes, the swizzle width) wide with the 128-byte
+// swizzle that the UMMA shared-memory descriptors expect; the store map of the GEMM
+// outputs moves 32 x 32 boxes. Host code.
 #pragma once
 
 #include <cstdint>
@@ -44,6 +45,24 @@ inline bool encode_map2(CUtensorMap* m, const void* base, uint64_t rows, uint64_
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Store map of a bf16 matrix [rows, cols] (cols contiguous): boxes of 32 cols (64 bytes)
+// x 32 rows with the 64-byte swizzle (16-byte chunk c of row r sits at chunk
+// c ^ ((r >> 1) & 3) of its 64-byte shared-memory row).
+constexpr uint32_t kStoreBoxCols = 32;
+constexpr uint32_t kStoreBoxRows = 32;
+inline bool encode_store_map2(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {kStoreBoxCols, kStoreBoxRows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
