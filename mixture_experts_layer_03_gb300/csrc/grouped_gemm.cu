@@ -67,6 +67,11 @@ constexpr int kTmemCols = 512;
 constexpr int kThreads = 192;
 constexpr int kMaxGroups = 257;
 constexpr int kSchedDepth = 4;                       // work indices in flight inside a CTA
+// Pair kernel: the first CTA claims its next unit this many K blocks before it has issued
+// the current unit's loads, so the claim's atomic latency stays off the load stream; a
+// whole unit ahead would lengthen the tail (faster pairs could no longer take more work).
+// (In the single-SM kernel the same early claim measured no gain.)
+constexpr int kClaimLead = 4;
 // Epilogue staging of both kernels: per epilogue warp two 32 x 32 bf16 boxes for TMA
 // stores, after the stage ring.
 constexpr int kStoreBufBytes = static_cast<int>(kStoreBoxRows * kStoreBoxCols * 2);
@@ -909,6 +914,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
       // ------------------------------------------------------------ TMA producer
       int fills = 0;
       bool ok = true;
+      int claimed = 0;            // the first CTA's claim for its next unit
+      bool have_claim = false;
       for (int it = 0; ok; ++it) {
         const int slot = it & (kSchedDepth - 1);
         const uint32_t sph = (it / kSchedDepth) & 1;
@@ -919,7 +926,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
             ok = false;
             break;
           }
-          unit = atomicAdd(a.sched, 1);
+          unit = have_claim ? claimed : atomicAdd(a.sched, 1);
+          have_claim = false;
           if (unit >= total) unit = -1;
           s_tile[slot] = unit;
           st_shared_cluster_u32(peer_s_tile + 4u * slot, static_cast<uint32_t>(unit));
@@ -949,7 +957,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
         const uint32_t xbytes = t.token_major ? kXStageBytes : static_cast<uint32_t>(half) * kRowBytes;
         const uint32_t tx_bytes = 2u * (xbytes + kWStageBytes);
         const int nkb = t.K / kBK;
+        const int claim_kb = nkb > kClaimLead ? nkb - kClaimLead : 0;
         for (int kb = 0; kb < nkb; ++kb) {
+          if (lead && kb == claim_kb) {
+            claimed = atomicAdd(a.sched, 1);
+            have_claim = true;
+          }
           const int stage = fills % kStages;
           if (!mbar_wait<true>(&empty_bar[stage], ((fills / kStages) & 1) ^ 1u, abort)) {
             flag_timeout(a.status, abort);
