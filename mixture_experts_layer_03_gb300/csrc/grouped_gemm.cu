@@ -136,14 +136,28 @@ __device__ __forceinline__ Unit decode_unit(int unit, const int32_t* s_off, cons
   const int left = m - (pairs << 8);
   const int nu = pairs + (left > 0);
   const int local = unit - s_off[g];
-  const int nt = local / nu;
-  const int u = local - nt * nu;
   const bool shared = g >= a.E;
   Unit t;
   t.g = g;
   t.K = shared ? a.K_shared : a.K_routed;
   t.N = shared ? a.N_shared : a.N_routed;
-  t.n0 = nt * (fc1 ? kFc1Cols : kFc2Cols);
+  // Order of the group's (row unit u, channel tile nt) grid. The pairs working at the
+  // same time should share their operands in L2, so the smaller of the two panels is
+  // kept resident: when the group's rows outnumber the expert's weight rows (FC1 2N,
+  // FC2 N), the row units go outer and every channel tile of a row unit follows it (the
+  // expert's weights stay in L2 and each A row block is read once); otherwise the
+  // channel tiles go outer (each weight tile stays in L2 while the row units pass).
+  const int cols = fc1 ? kFc1Cols : kFc2Cols;
+  int nt, u;
+  if (m >= (fc1 ? 2 : 1) * t.N) {
+    const int nnt = (t.N + cols - 1) / cols;
+    u = local / nnt;
+    nt = local - u * nnt;
+  } else {
+    nt = local / nu;
+    u = local - nt * nu;
+  }
+  t.n0 = nt * cols;
   t.narrow = 0;
   if (u < pairs || left > 128) {
     // Two row tiles, one per CTA; for the leftover unit (129..255 rows) the second tile
