@@ -110,7 +110,7 @@ typedef struct {
   size_t offsets;     /* int32[E+1]: exclusive scan of the routed counts                     */
   size_t tile_off1;   /* int32[2][G+1]: FC1 offsets per group, CTA-pair list then single-SM  */
   size_t tile_off2;   /* int32[2][G+1]: FC2 offsets per group, CTA-pair list then single-SM  */
-  size_t sched;       /* int32[8]: work-claim and finish counters of the four GEMM launches    */
+  size_t sched;       /* int32[8 + G]: GEMM work-claim/finish counters, then per-group FC1 done  */
   size_t block_hist;  /* int32[nb*E]: per-chunk expert histograms                            */
   size_t perm_src;    /* int32[T*k]: permuted row -> flat index f = t*k + j                  */
   size_t perm_inv;    /* int32[T*k]: flat index -> permuted row (-1 if the id was invalid)   */

@@ -99,7 +99,7 @@ bool compute_layout(const moe_problem& p, moe_ws_layout* out) {
   L.offsets = o;     o = align_up(o + 4 * size_t(p.E + 1), A);
   L.tile_off1 = o;   o = align_up(o + 8 * size_t(G + 1), A);
   L.tile_off2 = o;   o = align_up(o + 8 * size_t(G + 1), A);
-  L.sched = o;       o = align_up(o + 32, A);
+  L.sched = o;       o = align_up(o + 4 * size_t(kSchedCounters + G), A);
   L.block_hist = o;  o = align_up(o + 4 * size_t(nb) * size_t(p.E), A);
   L.perm_src = o;    o = align_up(o + 4 * size_t(P), A);
   L.perm_inv = o;    o = align_up(o + 4 * size_t(P), A);
@@ -278,8 +278,7 @@ moe_status moe_forward_partial(const moe_problem* p, int32_t e_lo, int32_t e_hi,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   if ((st = launch_permute(*p, L, x, ids, e_lo, e_hi, ws, s)) != MOE_OK) return st;
-  if ((st = launch_fc1(*p, L, w13, w13_s, e_lo, e_hi, ws, s)) != MOE_OK) return st;
-  if ((st = launch_fc2(*p, L, w2, w2_s, e_lo, e_hi, ws, s)) != MOE_OK) return st;
+  if ((st = launch_fc12(*p, L, w13, w13_s, w2, w2_s, e_lo, e_hi, ws, s)) != MOE_OK) return st;
   return launch_finalize(*p, L, scales, shared_gate, y, ws, s);
 }
 
@@ -352,8 +351,7 @@ moe_status moe_forward_static(const moe_problem* p, const void* x, const int32_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The permute step clears the status word and the GEMM tile counters in the scratch.
   if ((st = launch_permute(*p, L, x, ids, 0, p->E, ws, s)) != MOE_OK) return st;
-  if ((st = launch_fc1(*p, L, w13, w13_s, 0, p->E, ws, s)) != MOE_OK) return st;
-  if ((st = launch_fc2(*p, L, w2, w2_s, 0, p->E, ws, s)) != MOE_OK) return st;
+  if ((st = launch_fc12(*p, L, w13, w13_s, w2, w2_s, 0, p->E, ws, s)) != MOE_OK) return st;
   return launch_finalize(*p, L, scales, nullptr, y, ws, s);
 }
 

@@ -100,6 +100,7 @@ struct GemmArgs {
   int64_t out_ld;
   int32_t* status;
   int32_t* sched;           // [0] next unit to claim, [1] CTAs finished (both reset at exit)
+  int32_t* dep;             // fused single-SM launch: [G] FC1 tiles finished per group
   int32_t planes;           // routed weight planes in the maps (experts of this call)
   int32_t prefetch_kb;      // narrow FC1: K blocks of its guessed first tile each CTA
                             // prefetches into L2 before the work lists exist (0: none)
@@ -456,18 +457,134 @@ __device__ __forceinline__ bool single_k_loop_narrow(uint32_t d, uint32_t idesc,
   return true;
 }
 
-// The single-SM kernel. kNarrow: a launch whose small groups get narrow weight-major
-// tiles (see narrow_max_rows); only that form reads the 64-row weight maps. The tensor
-// maps are kernel parameters (__grid_constant__), passed here by address.
+// Tensor maps of one GEMM for the single-SM kernel: addresses of the kernel's
+// __grid_constant__ parameters.
+struct SingleMaps {
+  const CUtensorMap* x128;   // A rows, box 64 x 128
+  const CUtensorMap* x16;    // A rows, box 64 x 16
+  const CUtensorMap* w;      // routed weights [planes, R, K], box 64 x 128
+  const CUtensorMap* ws;     // shared weights [1, R, K]
+  const CUtensorMap* w64;    // routed, box 64 x 64 (narrow launches only)
+  const CUtensorMap* ws64;   // shared, box 64 x 64 (narrow launches only)
+  const CUtensorMap* out;    // output rows, store box 32 x 32
+};
+
+// What a single-SM launch runs: one GEMM, or both (FC1's work list, then FC2's).
+constexpr int kModeFc2 = 0;
+constexpr int kModeFc1 = 1;
+constexpr int kModeFused = 2;
+
+// Producer of the single-SM kernel: the TMA loads of one tile, stage by stage. Returns
+// false if a stage did not come free in time.
 template <bool kFc1, bool kNarrow>
-__device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128,  // A, box 64 x 128
-                                                   const CUtensorMap* map_x16,   // A, box 64 x 16
-                                                   const CUtensorMap* map_w,     // routed [E, R, K]
-                                                   const CUtensorMap* map_ws,    // shared [1, R, K]
-                                                   const CUtensorMap* map_w64,   // routed, 64 rows
-                                                   const CUtensorMap* map_ws64,  // shared, 64 rows
-                                                   const CUtensorMap* map_out,   // output, 32 x 32
-                                                   const GemmArgs& a) {
+__device__ __forceinline__ bool single_produce(const Unit& t, const SingleMaps& m,
+                                               const GemmArgs& a, int& stage, uint32_t& phase,
+                                               int& issued, uint8_t* sX, uint8_t* sW,
+                                               uint64_t* full_bar, uint64_t* empty_bar,
+                                               volatile int* abort) {
+  const bool shared = t.g >= a.E;
+  const CUtensorMap* mw = shared ? m.ws : m.w;
+  const int ecoord = shared ? 0 : t.g - a.plane_off;
+  const int wr0 = t.n0;
+  const int wr1 = kFc1 ? (t.N + t.n0) : (t.n0 + 128);
+  const uint32_t xbytes = static_cast<uint32_t>(t.ntok) * kRowBytes;
+  const uint32_t bytes = (2 * kWStageBytes) + (t.token_major ? kXStageBytes : xbytes);
+  const int nkb = t.K / kBK;
+  // Narrow tiles: two K blocks per stage; FC1 W blocks are 64 gate rows (64-row boxes)
+  // then the 64 up rows, FC2 W blocks 128 channel rows.
+  const CUtensorMap* mwn = kFc1 ? (shared ? m.ws64 : m.w64) : mw;
+  const int nst = kNarrow && t.narrow ? (nkb + 1) >> 1 : nkb;
+  for (int j = 0; j < nst; ++j) {
+    if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort)) return false;
+    uint8_t* xs = sX + stage * kXStageBytes;
+    uint8_t* ws = sW + stage * (2 * kWStageBytes);
+    if (kNarrow && t.narrow) {
+      const int nk = nkb - 2 * j < 2 ? 1 : 2;
+      mbar_arrive_expect_tx(&full_bar[stage], nk * (kWStageBytes + xbytes));
+      for (int b = 0; b < nk; ++b) {
+        const int kc = (2 * j + b) * kBK;
+        uint8_t* xb = xs + b * (kXStageBytes / 2);
+        uint8_t* wb = ws + b * kWStageBytes;
+        for (int r = 0; r < t.ntok; r += 16)
+          tma_load_2d(xb + r * kRowBytes, m.x16, &full_bar[stage], kc, t.row0 + r);
+        if (kFc1) {
+          tma_load_3d(wb, mwn, &full_bar[stage], kc, t.n0, ecoord);
+          tma_load_3d(wb + kWStageBytes / 2, mwn, &full_bar[stage], kc, t.N + t.n0, ecoord);
+        } else {
+          tma_load_3d(wb, mwn, &full_bar[stage], kc, t.n0, ecoord);
+        }
+      }
+    } else {
+      mbar_arrive_expect_tx(&full_bar[stage], bytes);
+      const int kc = j * kBK;
+      if (t.token_major) {
+        tma_load_2d(xs, m.x128, &full_bar[stage], kc, t.row0);
+      } else {
+        for (int r = 0; r < t.ntok; r += 16)
+          tma_load_2d(xs + r * kRowBytes, m.x16, &full_bar[stage], kc, t.row0 + r);
+      }
+      tma_load_3d(ws, mw, &full_bar[stage], kc, wr0, ecoord);
+      tma_load_3d(ws + kWStageBytes, mw, &full_bar[stage], kc, wr1, ecoord);
+    }
+    ++issued;
+    if (++stage == kSingleStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+  return true;
+}
+
+// Epilogue of one single-SM tile, by the four epilogue warps (q = TMEM lane quarter).
+template <bool kFc1, bool kNarrow>
+__device__ __forceinline__ void single_epilogue(uint32_t tb, const Unit& t, int q, int lane,
+                                                uint8_t* my_out, int& sbuf, float* s_xchg,
+                                                const SingleMaps& m, const GemmArgs& a) {
+  const int lrow = q * 32 + lane;
+  if (kNarrow && t.narrow) {
+    // Lane = weight row of the narrow tile (FC1: gate lanes 0-63, up lanes 64-127).
+    store_weight_major<kFc1>(tb, t, lrow, 0u, s_xchg, a);
+  } else if (t.token_major) {
+    // Thread = token row lrow; columns = channels (a full 128-row tile).
+    store_token_major_tma<kFc1>(tb, t, q, lane, my_out, sbuf, m.out);
+  } else {
+    // Thread = channel lrow (of the 128 in D0, and of D1); columns = tokens.
+    float va[16], vb[16];
+    const int ch0 = t.n0 + lrow;
+    const int ch1 = kFc1 ? ch0 : (t.n0 + 128 + lrow);
+    const bool v0 = ch0 < t.N, v1 = ch1 < t.N;
+#pragma unroll 1
+    for (int c0 = 0; c0 < t.ntok; c0 += 16) {
+      tmem_ld2_x16(tb + c0, tb + 128 + c0, va, vb);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int r = c0 + i;
+        if (r < t.rows) {
+          __nv_bfloat16* orow = a.out + static_cast<int64_t>(t.row0 + r) * a.out_ld;
+          if (kFc1) {
+            if (v0) orow[ch0] = __float2bfloat16_rn(silu(va[i]) * vb[i]);
+          } else {
+            if (v0) orow[ch0] = __float2bfloat16_rn(va[i]);
+            if (v1) orow[ch1] = __float2bfloat16_rn(vb[i]);
+          }
+        }
+      }
+    }
+  }
+}
+
+// The single-SM kernel. kNarrow: a launch whose small groups get narrow weight-major
+// tiles (see narrow_max_rows); only that form reads the 64-row weight maps. kMode: FC1
+// alone (m1, a1), FC2 alone (m2, a2; the callers pass the same maps and arguments twice),
+// or both GEMMs in one persistent launch: the work list is FC1's tiles, then FC2's, claimed
+// from one counter. A fused FC2 tile of group g first waits (bounded) until every FC1 tile
+// of group g has stored its h rows: each FC1 tile's epilogue adds 1 to the group's
+// completion counter (a1.dep[g]) once its stores are visible. Tiles are claimed in list
+// order and every claimed FC1 tile completes without waiting on FC2 work, so the waits
+// end; FC2 starts on SMs that FC1's last round leaves idle, with no second launch.
+template <int kMode, bool kNarrow>
+__device__ __forceinline__ void single_kernel_body(const SingleMaps& m1, const SingleMaps& m2,
+                                                   const GemmArgs& a1, const GemmArgs& a2) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kSingleStages], empty_bar[kSingleStages];
   __shared__ float s_xchg[kNarrow ? 64 * kXchgStride : 1];
@@ -476,7 +593,10 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
   __shared__ int s_tile[kSchedDepth];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
-  __shared__ int32_t s_off[kMaxGroups + 1], s_cnt[kMaxGroups], s_start[kMaxGroups];
+  __shared__ int32_t s_off1[kMode == kModeFc2 ? 1 : kMaxGroups + 1];
+  __shared__ int32_t s_off2[kMode == kModeFc1 ? 1 : kMaxGroups + 1];
+  __shared__ int32_t s_cnt[kMaxGroups], s_start[kMaxGroups];
+  constexpr bool kFused = kMode == kModeFused;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -507,30 +627,40 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_map(map_x128);
-    tma_prefetch_map(map_x16);
-    tma_prefetch_map(map_w);
-    tma_prefetch_map(map_ws);
-    tma_prefetch_map(map_out);
-    if (kFc1 && kNarrow) {
-      tma_prefetch_map(map_w64);
-      tma_prefetch_map(map_ws64);
+    if (kMode != kModeFc2) {
+      tma_prefetch_map(m1.x128);
+      tma_prefetch_map(m1.x16);
+      tma_prefetch_map(m1.w);
+      tma_prefetch_map(m1.ws);
+      tma_prefetch_map(m1.out);
+    }
+    if (kMode != kModeFc1) {
+      tma_prefetch_map(m2.x128);
+      tma_prefetch_map(m2.x16);
+      tma_prefetch_map(m2.w);
+      tma_prefetch_map(m2.ws);
+      tma_prefetch_map(m2.out);
+    }
+    if (kNarrow && kMode != kModeFc1) tma_prefetch_map(m2.w64);
+    if (kNarrow && kMode != kModeFc2) {
+      tma_prefetch_map(m1.w64);
+      tma_prefetch_map(m1.ws64);
       // The kernels before this one (routing and the permutation) leave HBM idle. Pull
       // this CTA's likely first tiles into L2 meanwhile: the claims of round r are list
       // entries r * gridDim.x .. (r + 1) * gridDim.x - 1, and with every expert active
       // entry b is expert b / tiles-per-expert, narrow tile b mod tiles-per-expert. A
       // wrong guess (an inactive expert) only costs idle bandwidth.
-      const int tpe = (a.N_routed + kFc1NarrowCols - 1) / kFc1NarrowCols;
-      const int nkb = a.K_routed / kBK;
-      int left = a.prefetch_kb;
+      const int tpe = (a1.N_routed + kFc1NarrowCols - 1) / kFc1NarrowCols;
+      const int nkb = a1.K_routed / kBK;
+      int left = a1.prefetch_kb;
       for (int b = static_cast<int>(blockIdx.x); left > 0; b += static_cast<int>(gridDim.x)) {
         const int g = b / tpe;
-        if (g >= a.planes) break;
+        if (g >= a1.planes) break;
         const int n0 = (b - g * tpe) * kFc1NarrowCols;
         const int n = left < nkb ? left : nkb;
         for (int kb = 0; kb < n; ++kb) {
-          tma_prefetch_3d(map_w64, kb * kBK, n0, g);
-          tma_prefetch_3d(map_w64, kb * kBK, a.N_routed + n0, g);
+          tma_prefetch_3d(m1.w64, kb * kBK, n0, g);
+          tma_prefetch_3d(m1.w64, kb * kBK, a1.N_routed + n0, g);
         }
         left -= n;
       }
@@ -542,17 +672,28 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
   }
   // Everything above overlaps the previous kernel; the work lists are its output.
   pdl_wait();
-  for (int i = threadIdx.x; i <= a.G; i += blockDim.x) s_off[i] = a.tile_off[i];
-  for (int i = threadIdx.x; i < a.G; i += blockDim.x) {
-    s_cnt[i] = a.counts[i];
-    s_start[i] = a.starts[i];
+  if (kMode != kModeFc2)
+    for (int i = threadIdx.x; i <= a1.G; i += blockDim.x) s_off1[i] = a1.tile_off[i];
+  if (kMode != kModeFc1)
+    for (int i = threadIdx.x; i <= a2.G; i += blockDim.x) s_off2[i] = a2.tile_off[i];
+  for (int i = threadIdx.x; i < a1.G; i += blockDim.x) {
+    s_cnt[i] = a1.counts[i];
+    s_start[i] = a1.starts[i];
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   volatile int* abort = &s_abort;
-  const int total = s_off[a.G];
+  const int total1 = kMode == kModeFc2 ? 0 : s_off1[a1.G];
+  const int total = total1 + (kMode == kModeFc1 ? 0 : s_off2[a2.G]);
+  // A claimed index -> (GEMM, tile). In the single-GEMM modes the branch is a constant.
+  auto is_fc1 = [&](int tile) { return kFused ? tile < total1 : kMode == kModeFc1; };
+  auto decode = [&](int tile, bool fc1) {
+    return fc1 ? decode_single(tile, s_off1, s_cnt, s_start, a1, true, kNarrow)
+               : decode_single(kFused ? tile - total1 : tile, s_off2, s_cnt, s_start, a2, false,
+                               kNarrow);
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -564,70 +705,32 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
       for (int it = 0; ok; ++it) {
         const int slot = it & (kSchedDepth - 1);
         if (!mbar_wait(&sched_empty[slot], ((it / kSchedDepth) & 1) ^ 1u, abort)) {
-          flag_timeout(a.status, abort);
+          flag_timeout(a1.status, abort);
           ok = false;
           break;
         }
-        int tile = atomicAdd(a.sched, 1);
+        int tile = atomicAdd(a1.sched, 1);
         if (tile >= total) tile = -1;
         s_tile[slot] = tile;
         mbar_arrive(&sched_full[slot]);
         if (tile < 0) break;
-        const Unit t = decode_single(tile, s_off, s_cnt, s_start, a, kFc1, kNarrow);
-        const bool shared = t.g >= a.E;
-        const CUtensorMap* mw = shared ? map_ws : map_w;
-        const int ecoord = shared ? 0 : t.g - a.plane_off;
-        const int wr0 = t.n0;
-        const int wr1 = kFc1 ? (t.N + t.n0) : (t.n0 + 128);
-        const uint32_t xbytes = static_cast<uint32_t>(t.ntok) * kRowBytes;
-        const uint32_t bytes = (2 * kWStageBytes) + (t.token_major ? kXStageBytes : xbytes);
-        const int nkb = t.K / kBK;
-        // Narrow tiles: two K blocks per stage; FC1 W blocks are 64 gate rows (64-row
-        // boxes) then the 64 up rows, FC2 W blocks 128 channel rows.
-        const CUtensorMap* mwn = kFc1 ? (shared ? map_ws64 : map_w64) : mw;
-        const int nst = kNarrow && t.narrow ? (nkb + 1) >> 1 : nkb;
-        for (int j = 0; j < nst; ++j) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort)) {
-            flag_timeout(a.status, abort);
-            ok = false;
-            break;
+        const bool fc1 = is_fc1(tile);
+        const Unit t = decode(tile, fc1);
+        if (fc1) {
+          ok = single_produce<true, kNarrow>(t, m1, a1, stage, phase, issued, sX, sW, full_bar,
+                                             empty_bar, abort);
+        } else {
+          if (kFused) {
+            // h rows of group g are complete once all its FC1 tiles have signalled; the
+            // TMA loads that follow read them through the async proxy.
+            ok = wait_count(a1.dep + t.g, s_off1[t.g + 1] - s_off1[t.g], abort);
+            fence_proxy_async_global();
           }
-          uint8_t* xs = sX + stage * kXStageBytes;
-          uint8_t* ws = sW + stage * (2 * kWStageBytes);
-          if (kNarrow && t.narrow) {
-            const int nk = nkb - 2 * j < 2 ? 1 : 2;
-            mbar_arrive_expect_tx(&full_bar[stage], nk * (kWStageBytes + xbytes));
-            for (int b = 0; b < nk; ++b) {
-              const int kc = (2 * j + b) * kBK;
-              uint8_t* xb = xs + b * (kXStageBytes / 2);
-              uint8_t* wb = ws + b * kWStageBytes;
-              for (int r = 0; r < t.ntok; r += 16)
-                tma_load_2d(xb + r * kRowBytes, map_x16, &full_bar[stage], kc, t.row0 + r);
-              if (kFc1) {
-                tma_load_3d(wb, mwn, &full_bar[stage], kc, t.n0, ecoord);
-                tma_load_3d(wb + kWStageBytes / 2, mwn, &full_bar[stage], kc, t.N + t.n0, ecoord);
-              } else {
-                tma_load_3d(wb, mwn, &full_bar[stage], kc, t.n0, ecoord);
-              }
-            }
-          } else {
-            mbar_arrive_expect_tx(&full_bar[stage], bytes);
-            const int kc = j * kBK;
-            if (t.token_major) {
-              tma_load_2d(xs, map_x128, &full_bar[stage], kc, t.row0);
-            } else {
-              for (int r = 0; r < t.ntok; r += 16)
-                tma_load_2d(xs + r * kRowBytes, map_x16, &full_bar[stage], kc, t.row0 + r);
-            }
-            tma_load_3d(ws, mw, &full_bar[stage], kc, wr0, ecoord);
-            tma_load_3d(ws + kWStageBytes, mw, &full_bar[stage], kc, wr1, ecoord);
-          }
-          ++issued;
-          if (++stage == kSingleStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          if (ok)
+            ok = single_produce<false, kNarrow>(t, m2, a2, stage, phase, issued, sX, sW,
+                                                full_bar, empty_bar, abort);
         }
+        if (!ok) flag_timeout(a1.status, abort);
       }
       if (!ok) {
         // Let the copies already in flight land before the CTA exits: wait (bounded)
@@ -657,16 +760,16 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
       for (int it = 0; ok; ++it) {
         const int slot = it & (kSchedDepth - 1);
         if (!mbar_wait(&sched_full[slot], (it / kSchedDepth) & 1, abort)) {
-          flag_timeout(a.status, abort);
+          flag_timeout(a1.status, abort);
           ok = false;
           break;
         }
         const int tile = *reinterpret_cast<volatile int*>(&s_tile[slot]);
         mbar_arrive(&sched_empty[slot]);
         if (tile < 0) break;
-        const Unit t = decode_single(tile, s_off, s_cnt, s_start, a, kFc1, kNarrow);
+        const Unit t = decode(tile, is_fc1(tile));
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort)) {
-          flag_timeout(a.status, abort);
+          flag_timeout(a1.status, abort);
           ok = false;
           break;
         }
@@ -683,7 +786,7 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
           ok = single_k_loop<false>(d, idesc_bf16_f32(128, t.ntok), nkb, stage, phase, sx0, sw0,
                                     full_bar, empty_bar, abort);
         if (!ok) {
-          flag_timeout(a.status, abort);
+          flag_timeout(a1.status, abort);
           break;
         }
         umma_commit(&tfull_bar[acc]);
@@ -702,7 +805,6 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quarter of this warp
-    const int lrow = q * 32 + lane;         // accumulator row (lane) of this thread
     uint8_t* my_out = sOut + q * 2 * kStoreBufBytes;
     int sbuf = 0;
     int acc = 0;
@@ -711,55 +813,40 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
       const int slot = it & (kSchedDepth - 1);
       const bool have = mbar_wait(&sched_full[slot], (it / kSchedDepth) & 1, abort);
       if (!__all_sync(0xffffffffu, have)) {
-        flag_timeout(a.status, abort);
+        flag_timeout(a1.status, abort);
         break;
       }
       const int tile = *reinterpret_cast<volatile int*>(&s_tile[slot]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sched_empty[slot]);
       if (tile < 0) break;
-      const Unit t = decode_single(tile, s_off, s_cnt, s_start, a, kFc1, kNarrow);
+      const bool fc1 = is_fc1(tile);
+      const Unit t = decode(tile, fc1);
       const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort);
       // Lanes may leave the poll at different times; tcgen05.ld is warp-collective.
       if (!__all_sync(0xffffffffu, got)) {
-        flag_timeout(a.status, abort);
+        flag_timeout(a1.status, abort);
         break;
       }
       tc_fence_after();
       const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * kAccCols) +
                           (static_cast<uint32_t>(q * 32) << 16);
-      float va[16], vb[16];
-      if (kNarrow && t.narrow) {
-        // Lane = weight row of the narrow tile (FC1: gate lanes 0-63, up lanes 64-127).
-        store_weight_major<kFc1>(tb, t, lrow, 0u, s_xchg, a);
-      } else if (t.token_major) {
-        // Thread = token row lrow; columns = channels (a full 128-row tile).
-        store_token_major_tma<kFc1>(tb, t, q, lane, my_out, sbuf, map_out);
-      } else {
-        // Thread = channel lrow (of the 128 in D0, and of D1); columns = tokens.
-        const int ch0 = t.n0 + lrow;
-        const int ch1 = kFc1 ? ch0 : (t.n0 + 128 + lrow);
-        const bool v0 = ch0 < t.N, v1 = ch1 < t.N;
-#pragma unroll 1
-        for (int c0 = 0; c0 < t.ntok; c0 += 16) {
-          tmem_ld2_x16(tb + c0, tb + 128 + c0, va, vb);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int r = c0 + i;
-            if (r < t.rows) {
-              __nv_bfloat16* orow = a.out + static_cast<int64_t>(t.row0 + r) * a.out_ld;
-              if (kFc1) {
-                if (v0) orow[ch0] = __float2bfloat16_rn(silu(va[i]) * vb[i]);
-              } else {
-                if (v0) orow[ch0] = __float2bfloat16_rn(va[i]);
-                if (v1) orow[ch1] = __float2bfloat16_rn(vb[i]);
-              }
-            }
-          }
-        }
-      }
+      if (fc1) single_epilogue<true, kNarrow>(tb, t, q, lane, my_out, sbuf, s_xchg, m1, a1);
+      else single_epilogue<false, kNarrow>(tb, t, q, lane, my_out, sbuf, s_xchg, m2, a2);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
+      if (kFused && fc1) {
+        // Publish this tile's h rows to the FC2 tiles of its group: every store of the
+        // four warps complete and visible (TMA stores: waited for, then a proxy fence),
+        // then one release add on the group's counter.
+        if (lane == 0) {
+          bulk_wait_group<0>();
+          fence_proxy_async_global();
+        }
+        __threadfence();
+        named_barrier_sync(2, 128);
+        if (q == 0 && lane == 0) red_release_gpu_add(a1.dep + t.g, 1);
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -775,7 +862,7 @@ __device__ __forceinline__ void single_kernel_body(const CUtensorMap* map_x128, 
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
-  if (threadIdx.x == 0) finish_claims(a);
+  if (threadIdx.x == 0) finish_claims(a1);
 }
 
 template <bool kFc1>
@@ -783,8 +870,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128, const __grid_constant__ CUtensorMap map_x16,
                     const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_ws,
                     const __grid_constant__ CUtensorMap map_out, GemmArgs a) {
-  single_kernel_body<kFc1, false>(&map_x128, &map_x16, &map_w, &map_ws, nullptr, nullptr, &map_out,
-                                  a);
+  const SingleMaps m{&map_x128, &map_x16, &map_w, &map_ws, nullptr, nullptr, &map_out};
+  single_kernel_body<kFc1 ? kModeFc1 : kModeFc2, false>(m, m, a, a);
 }
 
 template <bool kFc1>
@@ -796,8 +883,31 @@ grouped_gemm_narrow_kernel(const __grid_constant__ CUtensorMap map_x128,
                            const __grid_constant__ CUtensorMap map_w64,
                            const __grid_constant__ CUtensorMap map_ws64,
                            const __grid_constant__ CUtensorMap map_out, GemmArgs a) {
-  single_kernel_body<kFc1, true>(&map_x128, &map_x16, &map_w, &map_ws, &map_w64, &map_ws64,
-                                 &map_out, a);
+  const SingleMaps m{&map_x128, &map_x16, &map_w, &map_ws, &map_w64, &map_ws64, &map_out};
+  single_kernel_body<kFc1 ? kModeFc1 : kModeFc2, true>(m, m, a, a);
+}
+
+// Both GEMMs in one launch (FC1's tiles, then FC2's): maps and arguments of FC1 (x_perm,
+// w13, h) then of FC2 (h, w2, out_perm).
+template <bool kNarrow>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_fused_kernel(const __grid_constant__ CUtensorMap f1_x128,
+                          const __grid_constant__ CUtensorMap f1_x16,
+                          const __grid_constant__ CUtensorMap f1_w,
+                          const __grid_constant__ CUtensorMap f1_ws,
+                          const __grid_constant__ CUtensorMap f1_w64,
+                          const __grid_constant__ CUtensorMap f1_ws64,
+                          const __grid_constant__ CUtensorMap f1_out,
+                          const __grid_constant__ CUtensorMap f2_x128,
+                          const __grid_constant__ CUtensorMap f2_x16,
+                          const __grid_constant__ CUtensorMap f2_w,
+                          const __grid_constant__ CUtensorMap f2_ws,
+                          const __grid_constant__ CUtensorMap f2_w64,
+                          const __grid_constant__ CUtensorMap f2_ws64,
+                          const __grid_constant__ CUtensorMap f2_out, GemmArgs a1, GemmArgs a2) {
+  const SingleMaps m1{&f1_x128, &f1_x16, &f1_w, &f1_ws, &f1_w64, &f1_ws64, &f1_out};
+  const SingleMaps m2{&f2_x128, &f2_x16, &f2_w, &f2_ws, &f2_w64, &f2_ws64, &f2_out};
+  single_kernel_body<kModeFused, kNarrow>(m1, m2, a1, a2);
 }
 
 // ============================================================== CTA-pair kernel
@@ -1145,6 +1255,12 @@ moe_status prepare_kernels(int* max_clusters) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kFc1>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess && kFc1)
+      e = cudaFuncSetAttribute(grouped_gemm_fused_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSingleSmemBytes);
+    if (e == cudaSuccess && kFc1)
+      e = cudaFuncSetAttribute(grouped_gemm_fused_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSingleSmemBytes);
     if (e != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     const int sms = device_sm_count();
@@ -1165,19 +1281,27 @@ moe_status prepare_kernels(int* max_clusters) {
   return MOE_OK;
 }
 
+// The tensor maps, arguments and work bounds of one GEMM.
+struct GemmSetup {
+  CUtensorMap mx128, mx8, mx16, mw128, mws128, mw64, mws64, mout;
+  GemmArgs pair, single;        // arguments of the pair and single-SM launches
+  int64_t pair_bound, single_bound;
+  bool narrow;
+  int max_clusters;
+};
+
 template <bool kFc1>
-moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void* w,
-                       const void* w_s, int e_lo, int e_hi, char* ws, cudaStream_t s) {
-  int max_clusters = 1;
-  moe_status st = prepare_kernels<kFc1>(&max_clusters);
+moe_status setup_gemm(const moe_problem& p, const moe_ws_layout& L, const void* w,
+                      const void* w_s, int e_lo, int e_hi, char* ws, GemmSetup* g) {
+  g->max_clusters = 1;
+  moe_status st = prepare_kernels<kFc1>(&g->max_clusters);
   if (st != MOE_OK) return st;
   const int64_t R = L.rows;
   const int has_shared = p.shared_I > 0;
-  CUtensorMap mx128, mx8, mx16, mw128, mws128, mw64, mws64, mout;
   const void* A = kFc1 ? static_cast<const void*>(ws + L.x_perm) : static_cast<const void*>(ws + L.h);
   const uint64_t a_cols = kFc1 ? static_cast<uint64_t>(p.H) : static_cast<uint64_t>(L.h_ld);
-  bool ok = encode_map2(&mx128, A, R, a_cols, 128) && encode_map2(&mx8, A, R, a_cols, 8) &&
-            encode_map2(&mx16, A, R, a_cols, 16);
+  bool ok = encode_map2(&g->mx128, A, R, a_cols, 128) && encode_map2(&g->mx8, A, R, a_cols, 8) &&
+            encode_map2(&g->mx16, A, R, a_cols, 16);
   // Weights [planes, rows, K]: FC1 w13 [E, 2I, H] (shared [1, 2Is, H]); FC2 w2 [E, H, I]
   // (shared [1, H, Is]).
   const uint64_t wr = kFc1 ? 2ull * p.I : static_cast<uint64_t>(p.H);
@@ -1186,14 +1310,17 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
   const uint64_t sk = kFc1 ? static_cast<uint64_t>(p.H) : static_cast<uint64_t>(p.shared_I);
   // Routed weights hold the experts [e_lo, e_hi) of this call only.
   const uint64_t planes = static_cast<uint64_t>(e_hi - e_lo);
-  ok = ok && encode_map3(&mw128, w, planes, wr, wk, 128) && encode_map3(&mw64, w, planes, wr, wk, 64);
+  ok = ok && encode_map3(&g->mw128, w, planes, wr, wk, 128) &&
+       encode_map3(&g->mw64, w, planes, wr, wk, 64);
   if (has_shared)
-    ok = ok && encode_map3(&mws128, w_s, 1, sr, sk, 128) && encode_map3(&mws64, w_s, 1, sr, sk, 64);
+    ok = ok && encode_map3(&g->mws128, w_s, 1, sr, sk, 128) &&
+         encode_map3(&g->mws64, w_s, 1, sr, sk, 64);
   else
-    ok = ok && encode_map3(&mws128, w, planes, wr, wk, 128) && encode_map3(&mws64, w, planes, wr, wk, 64);
+    ok = ok && encode_map3(&g->mws128, w, planes, wr, wk, 128) &&
+         encode_map3(&g->mws64, w, planes, wr, wk, 64);
   // Output rows: FC1 h [R, h_ld], FC2 out_perm [R, H].
   const uint64_t out_cols = kFc1 ? static_cast<uint64_t>(L.h_ld) : static_cast<uint64_t>(p.H);
-  ok = ok && encode_store_map2(&mout, ws + (kFc1 ? L.h : L.out_perm), R, out_cols);
+  ok = ok && encode_store_map2(&g->mout, ws + (kFc1 ? L.h : L.out_perm), R, out_cols);
   if (!ok) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
   GemmArgs a;
@@ -1218,11 +1345,18 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
     a.out_ld = p.H;
   }
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
+  a.dep = nullptr;
   a.planes = e_hi - e_lo;
   a.prefetch_kb = 0;
   // Work lists [pair units | single-SM tiles], each G+1 offsets; counters [pair | single].
   const int32_t* lists = reinterpret_cast<const int32_t*>(ws + (kFc1 ? L.tile_off1 : L.tile_off2));
   int32_t* sched = reinterpret_cast<int32_t*>(ws + L.sched) + (kFc1 ? 0 : 4);
+  g->pair = a;
+  g->pair.tile_off = lists;
+  g->pair.sched = sched;
+  g->single = a;
+  g->single.tile_off = lists + (L.groups + 1);
+  g->single.sched = sched + 2;
 
   // One of the two kernels takes every group (see pair_min_rows). Upper bounds on its
   // work per channel tile: pair units at most R/256 + G, single-SM tiles at most
@@ -1230,44 +1364,48 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
   const int nI = has_shared && p.shared_I > p.I ? p.shared_I : p.I;
   const int64_t n_nt = kFc1 ? (nI + kFc1Cols - 1) / kFc1Cols : (p.H + kFc2Cols - 1) / kFc2Cols;
   const bool use_pairs = pair_min_rows(p) <= 2 * kTileRows;
-  const int64_t pair_bound = use_pairs ? (R / 256 + L.groups) * n_nt : 0;
+  g->pair_bound = use_pairs ? (R / 256 + L.groups) * n_nt : 0;
   // (A narrow tile is half a channel tile wide: at most twice as many tiles.)
-  const bool narrow = narrow_max_rows(p) > 0;
-  const int64_t single_bound =
-      use_pairs ? 0 : (narrow ? 2 : 1) * (R / kTileRows + L.groups) * n_nt;
+  g->narrow = narrow_max_rows(p) > 0;
+  g->single_bound = use_pairs ? 0 : (g->narrow ? 2 : 1) * (R / kTileRows + L.groups) * n_nt;
+  return MOE_OK;
+}
 
+// Narrow FC1: L2 prefetch of each CTA's guessed first tiles (see the kernel),
+// kPrefetchBytes over the grid: two 64-row boxes (16 KB) per K block.
+int32_t narrow_prefetch_kb(int64_t grid) {
+  const int64_t per_kb = 2 * 64 * kRowBytes;
+  const int64_t kb = kPrefetchBytes / (grid * per_kb);
+  return static_cast<int32_t>(kb < (1 << 20) ? kb : (1 << 20));
+}
+
+template <bool kFc1>
+moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void* w,
+                       const void* w_s, int e_lo, int e_hi, char* ws, cudaStream_t s) {
+  GemmSetup g;
+  moe_status st = setup_gemm<kFc1>(p, L, w, w_s, e_lo, e_hi, ws, &g);
+  if (st != MOE_OK) return st;
   cudaError_t err = cudaSuccess;
-  if (single_bound > 0) {
-    GemmArgs as = a;
-    as.tile_off = lists + (L.groups + 1);
-    as.sched = sched + 2;
+  if (g.single_bound > 0) {
+    GemmArgs as = g.single;
     int64_t grid = device_sm_count();
-    if (grid > single_bound) grid = single_bound;
+    if (grid > g.single_bound) grid = g.single_bound;
     if (grid < 1) grid = 1;
-    if (kFc1 && narrow) {
-      // L2 prefetch of each CTA's guessed first tiles (see the kernel), kPrefetchBytes
-      // over the grid: two 64-row boxes (16 KB) per K block.
-      const int64_t per_kb = 2 * 64 * kRowBytes;
-      const int64_t kb = kPrefetchBytes / (grid * per_kb);
-      as.prefetch_kb = static_cast<int32_t>(kb < (1 << 20) ? kb : (1 << 20));
-    }
-    if (narrow)
+    if (kFc1 && g.narrow) as.prefetch_kb = narrow_prefetch_kb(grid);
+    if (g.narrow)
       err = launch_pdl(grouped_gemm_narrow_kernel<kFc1>, dim3(static_cast<unsigned>(grid)),
-                       dim3(kThreads), kSingleSmemBytes, s, mx128, mx16, mw128, mws128, mw64, mws64,
-                       mout, as);
+                       dim3(kThreads), kSingleSmemBytes, s, g.mx128, g.mx16, g.mw128, g.mws128,
+                       g.mw64, g.mws64, g.mout, as);
     else
       err = launch_pdl(grouped_gemm_kernel<kFc1>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
-                       kSingleSmemBytes, s, mx128, mx16, mw128, mws128, mout, as);
+                       kSingleSmemBytes, s, g.mx128, g.mx16, g.mw128, g.mws128, g.mout, as);
   }
-  if (err == cudaSuccess && pair_bound > 0) {
-    GemmArgs ap = a;
-    ap.tile_off = lists;
-    ap.sched = sched;
-    int64_t clusters = max_clusters;
-    if (clusters > pair_bound) clusters = pair_bound;
+  if (err == cudaSuccess && g.pair_bound > 0) {
+    int64_t clusters = g.max_clusters;
+    if (clusters > g.pair_bound) clusters = g.pair_bound;
     err = launch_pdl(grouped_gemm_pair_kernel<kFc1>, dim3(static_cast<unsigned>(2 * clusters)),
-                     dim3(kThreads), kSmemBytes, s, mx128, mx8, mw128, mws128, mw64, mws64, mout,
-                     ap);
+                     dim3(kThreads), kSmemBytes, s, g.mx128, g.mx8, g.mw128, g.mws128, g.mw64,
+                     g.mws64, g.mout, g.pair);
   }
   if (err != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "grouped_gemm launch: %s", cudaGetErrorString(err));
@@ -1284,6 +1422,45 @@ moe_status launch_fc1(const moe_problem& p, const moe_ws_layout& L, const void* 
 moe_status launch_fc2(const moe_problem& p, const moe_ws_layout& L, const void* w2,
                       const void* w2_s, int e_lo, int e_hi, char* ws, cudaStream_t s) {
   return launch_gemm<false>(p, L, w2, w2_s, e_lo, e_hi, ws, s);
+}
+
+moe_status launch_fc12(const moe_problem& p, const moe_ws_layout& L, const void* w13,
+                       const void* w13_s, const void* w2, const void* w2_s, int e_lo, int e_hi,
+                       char* ws, cudaStream_t s) {
+  GemmSetup g1, g2;
+  moe_status st = setup_gemm<true>(p, L, w13, w13_s, e_lo, e_hi, ws, &g1);
+  if (st == MOE_OK) st = setup_gemm<false>(p, L, w2, w2_s, e_lo, e_hi, ws, &g2);
+  if (st != MOE_OK) return st;
+  if (g1.single_bound == 0 || g2.single_bound == 0) {
+    // CTA-pair sizes: two launches.
+    st = launch_gemm<true>(p, L, w13, w13_s, e_lo, e_hi, ws, s);
+    if (st == MOE_OK) st = launch_gemm<false>(p, L, w2, w2_s, e_lo, e_hi, ws, s);
+    return st;
+  }
+  // One persistent single-SM launch for both GEMMs: FC1's counter serves the joint list
+  // and the per-group completion counters follow the work counters.
+  GemmArgs a1 = g1.single, a2 = g2.single;
+  a1.dep = reinterpret_cast<int32_t*>(ws + L.sched) + kSchedCounters;
+  a2.dep = a1.dep;
+  a2.sched = a1.sched;
+  int64_t grid = device_sm_count();
+  if (grid > g1.single_bound + g2.single_bound) grid = g1.single_bound + g2.single_bound;
+  if (grid < 1) grid = 1;
+  if (g1.narrow) a1.prefetch_kb = narrow_prefetch_kb(grid);
+  cudaError_t err;
+  if (g1.narrow)
+    err = launch_pdl(grouped_gemm_fused_kernel<true>, dim3(static_cast<unsigned>(grid)),
+                     dim3(kThreads), kSingleSmemBytes, s, g1.mx128, g1.mx16, g1.mw128, g1.mws128,
+                     g1.mw64, g1.mws64, g1.mout, g2.mx128, g2.mx16, g2.mw128, g2.mws128, g2.mw64,
+                     g2.mws64, g2.mout, a1, a2);
+  else
+    err = launch_pdl(grouped_gemm_fused_kernel<false>, dim3(static_cast<unsigned>(grid)),
+                     dim3(kThreads), kSingleSmemBytes, s, g1.mx128, g1.mx16, g1.mw128, g1.mws128,
+                     g1.mw64, g1.mws64, g1.mout, g2.mx128, g2.mx16, g2.mw128, g2.mws128, g2.mw64,
+                     g2.mws64, g2.mout, a1, a2);
+  if (err != cudaSuccess)
+    return set_error(MOE_ERR_CUDA, "grouped_gemm launch: %s", cudaGetErrorString(err));
+  return MOE_OK;
 }
 
 }  // namespace moe

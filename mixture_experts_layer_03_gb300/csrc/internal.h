@@ -13,6 +13,12 @@ namespace moe {
 constexpr int kPermChunk = 1024;
 constexpr int kPermThreads = 512;
 
+// The workspace's sched region: kSchedCounters grouped-GEMM work counters (FC1 pair,
+// FC1 single, FC2 pair, FC2 single: a claim counter and a finished-CTA count each), then,
+// for the launch that runs both GEMMs, one FC1-tiles-finished counter per group. The
+// permute step zeroes all of them every forward.
+constexpr int kSchedCounters = 8;
+
 // Grouped GEMM tiling.
 constexpr int kTileRows = 128;    // token rows of a full (token-major) tile
 constexpr int kFc1Cols = 128;     // FC1 output channels per tile (gate and up each)
@@ -71,6 +77,13 @@ moe_status launch_fc1(const moe_problem& p, const moe_ws_layout& L, const void* 
 
 moe_status launch_fc2(const moe_problem& p, const moe_ws_layout& L, const void* w2,
                       const void* w2_s, int e_lo, int e_hi, char* ws, cudaStream_t s);
+
+// FC1 then FC2 of one forward. When the single-SM kernel tiles the groups, one persistent
+// launch runs both work lists (FC2 tiles wait for their group's FC1 tiles); at CTA-pair
+// sizes, the two launches of launch_fc1 and launch_fc2.
+moe_status launch_fc12(const moe_problem& p, const moe_ws_layout& L, const void* w13,
+                       const void* w13_s, const void* w2, const void* w2_s, int e_lo, int e_hi,
+                       char* ws, cudaStream_t s);
 
 // shared_gate: fp32 [T] gate logits of the shared expert (weight sigmoid) or NULL (1).
 moe_status launch_finalize(const moe_problem& p, const moe_ws_layout& L, const float* scales,

@@ -98,7 +98,7 @@ struct PlanArgs {
   int32_t* perm_src;   // [P]
   int32_t* perm_inv;   // [P]
   int32_t* status;
-  int32_t* sched;      // [8] grouped-GEMM work counters, zeroed here every forward
+  int32_t* sched;      // [kSchedCounters + G] grouped-GEMM counters, zeroed here every forward
 };
 
 // kSingleChunk: the whole problem is one chunk (one block); the block counts its own
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
       a.tile_off2[G] = t_p2;
       a.tile_off2[2 * G + 1] = t_s2;
     }
-    if (tid < 8) a.sched[tid] = 0;
+    for (int i = tid; i < kSchedCounters + G; i += blockDim.x) a.sched[i] = 0;
   }
   __syncthreads();
 

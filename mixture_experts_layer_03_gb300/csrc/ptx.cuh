@@ -181,6 +181,38 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's async-proxy (TMA) global accesses with its generic-proxy ones: after
+// a completed TMA store and before a release, or after an acquire and before a TMA load.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int32_t* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until *counter >= need (acquire). Gives up (returns false) after kWaitLimitNs or
+// as soon as *abort becomes non-zero.
+__device__ __forceinline__ bool wait_count(const int32_t* counter, int need, volatile int* abort) {
+  if (ld_acquire_gpu(counter) >= need) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      __nanosleep(128);
+      if (ld_acquire_gpu(counter) >= need) return true;
+    }
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // 3-D tiled load: box at (c0 innermost, c1 row, c2 matrix index).
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t c0, int32_t c1, int32_t c2) {
