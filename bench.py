@@ -219,10 +219,9 @@ def run_ours(args, rank, world):
         moe.moe_forward(xx, ids, sc, w13, w2, w13s, w2s, y=y, workspace=ws, stream=s)
 
     # route; permute (the histogram kernel only with more than one 1024-pair chunk, the
-    # plan kernel, the row gather); FC1 and FC2 (two CTA-pair launches when T*k >= 256*E,
-    # else one single-SM launch running both); finalize
-    gemm_launches = 2 if w.T * w.k >= 256 * w.E else 1
-    launches_per_step = 1 + (3 if ws.layout["n_chunks"] > 1 else 2) + gemm_launches + 1
+    # plan kernel, the row gather); FC1 and FC2 in one persistent GEMM launch (CTA-pair
+    # kernel when T*k >= 256*E, else single-SM); finalize
+    launches_per_step = 1 + (3 if ws.layout["n_chunks"] > 1 else 2) + 1 + 1
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()

@@ -942,16 +942,97 @@ __device__ __forceinline__ bool pair_k_loop(uint32_t d, uint32_t idesc, int nkb,
   return true;
 }
 
+// Tensor maps of one GEMM for the pair kernel: addresses of the kernel's __grid_constant__
+// parameters.
+struct PairMaps {
+  const CUtensorMap* x128;   // A rows, box 64 x 128
+  const CUtensorMap* x8;     // A rows, box 64 x 8
+  const CUtensorMap* w128;   // routed weights, box 64 x 128
+  const CUtensorMap* ws128;  // shared weights, box 64 x 128
+  const CUtensorMap* w64;    // routed weights, box 64 x 64
+  const CUtensorMap* ws64;   // shared weights, box 64 x 64
+  const CUtensorMap* out;    // output rows, store box 32 x 32
+};
+
+// Producer of one CTA of the pair: the TMA loads of one unit, K block by K block. The
+// first CTA also claims the pair's next unit kClaimLead K blocks before the end (from
+// *sched, into claimed / have_claim). Returns false if a stage did not come free in time.
 template <bool kFc1>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A rows, box 64 x 128
-                    const __grid_constant__ CUtensorMap map_x8,    // A rows, box 64 x 8
-                    const __grid_constant__ CUtensorMap map_w128,  // routed weights, box 64 x 128
-                    const __grid_constant__ CUtensorMap map_ws128, // shared weights, box 64 x 128
-                    const __grid_constant__ CUtensorMap map_w64,   // routed weights, box 64 x 64
-                    const __grid_constant__ CUtensorMap map_ws64,  // shared weights, box 64 x 64
-                    const __grid_constant__ CUtensorMap map_out,   // output rows, store box 32 x 32
-                    GemmArgs a) {
+__device__ __forceinline__ bool pair_produce(const Unit& t, const PairMaps& m, const GemmArgs& a,
+                                             uint32_t rank, bool lead, int32_t* sched,
+                                             int& claimed, bool& have_claim, int& fills,
+                                             uint8_t* sX, uint8_t* sW, uint32_t lead_full,
+                                             uint64_t* full_bar, uint64_t* empty_bar,
+                                             volatile int* abort) {
+  const bool shared = t.g >= a.E;
+  const CUtensorMap* mw128 = shared ? m.ws128 : m.w128;
+  const CUtensorMap* mw64 = shared ? m.ws64 : m.w64;
+  const int ecoord = shared ? 0 : t.g - a.plane_off;
+  const int r = static_cast<int>(rank);
+  // This CTA's token rows and its share of the weight rows.
+  const int half = t.ntok >> 1;
+  const int xrow = t.token_major ? t.row0 : t.row0 + r * half;
+  // Weight-major units have at most 128 token rows: each CTA loads its <= 64 rows in
+  // 8-row boxes (the same byte count in both CTAs).
+  const uint32_t xbytes = t.token_major ? kXStageBytes : static_cast<uint32_t>(half) * kRowBytes;
+  const uint32_t tx_bytes = 2u * (xbytes + kWStageBytes);
+  const int nkb = t.K / kBK;
+  const int claim_kb = nkb > kClaimLead ? nkb - kClaimLead : 0;
+  for (int kb = 0; kb < nkb; ++kb) {
+    if (lead && kb == claim_kb) {
+      claimed = atomicAdd(sched, 1);
+      have_claim = true;
+    }
+    const int stage = fills % kStages;
+    if (!mbar_wait<true>(&empty_bar[stage], ((fills / kStages) & 1) ^ 1u, abort)) return false;
+    if (lead) mbar_arrive_expect_tx(&full_bar[stage], tx_bytes);
+    const int kc = kb * kBK;
+    const uint32_t fb = lead_full + 8u * stage;
+    uint8_t* xs = sX + stage * kXStageBytes;
+    uint8_t* wsm = sW + stage * kWStageBytes;
+    if (t.token_major) {
+      tma_load_2d_pair(xs, m.x128, fb, kc, xrow);
+      const int wrow = kFc1 ? (lead ? t.n0 : t.N + t.n0) : (t.n0 + 128 * r);
+      tma_load_3d_pair(wsm, mw128, fb, kc, wrow, ecoord);
+    } else {
+      for (int q = 0; q < half; q += 8)
+        tma_load_2d_pair(xs + q * kRowBytes, m.x8, fb, kc, xrow + q);
+      if (kFc1) {
+        tma_load_3d_pair(wsm, mw64, fb, kc, t.n0 + 64 * r, ecoord);
+        tma_load_3d_pair(wsm + 64 * kRowBytes, mw64, fb, kc, t.N + t.n0 + 64 * r, ecoord);
+      } else {
+        tma_load_3d_pair(wsm, mw128, fb, kc, t.n0 + 128 * r, ecoord);
+      }
+    }
+    ++fills;
+  }
+  return true;
+}
+
+// Epilogue of one pair unit in one CTA, by its four epilogue warps.
+template <bool kFc1>
+__device__ __forceinline__ void pair_epilogue(uint32_t tb, const Unit& t, int q, int lane,
+                                              uint32_t rank, uint8_t* my_out, int& sbuf,
+                                              float* s_xchg, const PairMaps& m,
+                                              const GemmArgs& a) {
+  const int lrow = q * 32 + lane;
+  if (t.token_major && t.rows == kTileRows)
+    store_token_major_tma<kFc1>(tb, t, q, lane, my_out, sbuf, m.out);
+  else if (t.token_major)
+    store_token_major<kFc1>(tb, t, lrow, a);
+  else
+    store_weight_major<kFc1>(tb, t, lrow, rank, s_xchg, a);
+}
+
+// The CTA-pair kernel body. kMode as in the single-SM kernel: FC1 alone (m1, a1), FC2
+// alone (m2, a2; the callers pass the same maps and arguments twice), or both GEMMs in
+// one launch, FC1's units then FC2's from one counter. In the fused form an FC2 unit of
+// group g waits (bounded) until both CTAs of every FC1 unit of group g have signalled
+// that their h rows are stored and visible; claims go in list order and FC1 units never
+// wait, so every wait ends.
+template <int kMode>
+__device__ __forceinline__ void pair_kernel_body(const PairMaps& m1, const PairMaps& m2,
+                                                 const GemmArgs& a1, const GemmArgs& a2) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
@@ -959,8 +1040,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
   __shared__ int s_tile[kSchedDepth];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
-  __shared__ int32_t s_off[kMaxGroups + 1], s_cnt[kMaxGroups], s_start[kMaxGroups];
+  __shared__ int32_t s_off1[kMode == kModeFc2 ? 1 : kMaxGroups + 1];
+  __shared__ int32_t s_off2[kMode == kModeFc1 ? 1 : kMaxGroups + 1];
+  __shared__ int32_t s_cnt[kMaxGroups], s_start[kMaxGroups];
   __shared__ float s_xchg[64 * kXchgStride];
+  constexpr bool kFused = kMode == kModeFused;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -996,13 +1080,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_map(&map_x128);
-    tma_prefetch_map(&map_x8);
-    tma_prefetch_map(&map_w128);
-    tma_prefetch_map(&map_ws128);
-    tma_prefetch_map(&map_w64);
-    tma_prefetch_map(&map_ws64);
-    tma_prefetch_map(&map_out);
+    const PairMaps* ms[2] = {&m1, &m2};
+    for (int i = (kMode == kModeFc2 ? 1 : 0); i < (kMode == kModeFc1 ? 1 : 2); ++i) {
+      tma_prefetch_map(ms[i]->x128);
+      tma_prefetch_map(ms[i]->x8);
+      tma_prefetch_map(ms[i]->w128);
+      tma_prefetch_map(ms[i]->ws128);
+      tma_prefetch_map(ms[i]->w64);
+      tma_prefetch_map(ms[i]->ws64);
+      tma_prefetch_map(ms[i]->out);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(&s_tmem_base, kTmemCols);   // collective with the other CTA's warp 1
@@ -1010,10 +1097,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
   }
   // Everything above overlaps the previous kernel; the work lists are its output.
   pdl_wait();
-  for (int i = threadIdx.x; i <= a.G; i += blockDim.x) s_off[i] = a.tile_off[i];
-  for (int i = threadIdx.x; i < a.G; i += blockDim.x) {
-    s_cnt[i] = a.counts[i];
-    s_start[i] = a.starts[i];
+  if (kMode != kModeFc2)
+    for (int i = threadIdx.x; i <= a1.G; i += blockDim.x) s_off1[i] = a1.tile_off[i];
+  if (kMode != kModeFc1)
+    for (int i = threadIdx.x; i <= a2.G; i += blockDim.x) s_off2[i] = a2.tile_off[i];
+  for (int i = threadIdx.x; i < a1.G; i += blockDim.x) {
+    s_cnt[i] = a1.counts[i];
+    s_start[i] = a1.starts[i];
   }
   tc_fence_before();
   __syncthreads();
@@ -1021,7 +1111,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   volatile int* abort = &s_abort;
-  const int total = s_off[a.G];
+  const int total1 = kMode == kModeFc2 ? 0 : s_off1[a1.G];
+  const int total = total1 + (kMode == kModeFc1 ? 0 : s_off2[a2.G]);
+  // A claimed index -> (GEMM, unit). In the single-GEMM modes the branch is a constant.
+  auto is_fc1 = [&](int unit) { return kFused ? unit < total1 : kMode == kModeFc1; };
+  auto decode = [&](int unit, bool fc1, uint32_t r) {
+    return fc1 ? decode_unit(unit, s_off1, s_cnt, s_start, a1, true, r)
+               : decode_unit(kFused ? unit - total1 : unit, s_off2, s_cnt, s_start, a2, false, r);
+  };
 
   const uint32_t lead_full = mapa_shared(smem_u32(&full_bar[0]), 0);
   const uint32_t lead_tempty = mapa_shared(smem_u32(&tempty_bar[0]), 0);
@@ -1038,7 +1135,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
       // ------------------------------------------------------------ TMA producer
       int fills = 0;
       bool ok = true;
-      int claimed = 0;            // the first CTA's claim for its next unit
+      // The first CTA claims each next unit kClaimLead K blocks before it has issued the
+      // current unit's loads, so the atomic's latency is hidden; a whole unit ahead would
+      // lengthen the tail.
+      int claimed = 0;
       bool have_claim = false;
       for (int it = 0; ok; ++it) {
         const int slot = it & (kSchedDepth - 1);
@@ -1046,11 +1146,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
         int unit;
         if (lead) {
           if (!mbar_wait<true>(&sched_empty[slot], sph ^ 1u, abort)) {
-            flag_timeout(a.status, abort);
+            flag_timeout(a1.status, abort);
             ok = false;
             break;
           }
-          unit = have_claim ? claimed : atomicAdd(a.sched, 1);
+          unit = have_claim ? claimed : atomicAdd(a1.sched, 1);
           have_claim = false;
           if (unit >= total) unit = -1;
           s_tile[slot] = unit;
@@ -1059,7 +1159,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
           mbar_arrive_cluster(peer_sched_full + 8u * slot);
         } else {
           if (!mbar_wait<true>(&sched_full[slot], sph, abort)) {
-            flag_timeout(a.status, abort);
+            flag_timeout(a1.status, abort);
             ok = false;
             break;
           }
@@ -1067,53 +1167,23 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
           release_slot(slot);
         }
         if (unit < 0) break;
-        const Unit t = decode_unit(unit, s_off, s_cnt, s_start, a, kFc1, rank);
-        const bool shared = t.g >= a.E;
-        const CUtensorMap* mw128 = shared ? &map_ws128 : &map_w128;
-        const CUtensorMap* mw64 = shared ? &map_ws64 : &map_w64;
-        const int ecoord = shared ? 0 : t.g - a.plane_off;
-        const int r = static_cast<int>(rank);
-        // This CTA's token rows and its share of the weight rows.
-        const int half = t.ntok >> 1;
-        const int xrow = t.token_major ? t.row0 : t.row0 + r * half;
-        // Weight-major units have at most 128 token rows: each CTA loads its <= 64 rows in
-        // 8-row boxes (the same byte count in both CTAs).
-        const uint32_t xbytes = t.token_major ? kXStageBytes : static_cast<uint32_t>(half) * kRowBytes;
-        const uint32_t tx_bytes = 2u * (xbytes + kWStageBytes);
-        const int nkb = t.K / kBK;
-        const int claim_kb = nkb > kClaimLead ? nkb - kClaimLead : 0;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (lead && kb == claim_kb) {
-            claimed = atomicAdd(a.sched, 1);
-            have_claim = true;
+        const bool fc1 = is_fc1(unit);
+        const Unit t = decode(unit, fc1, rank);
+        if (fc1) {
+          ok = pair_produce<true>(t, m1, a1, rank, lead, a1.sched, claimed, have_claim, fills,
+                                  sX, sW, lead_full, full_bar, empty_bar, abort);
+        } else {
+          if (kFused) {
+            // Both CTAs of every FC1 unit of group g signal once their h rows are stored;
+            // the TMA loads that follow read those rows through the async proxy.
+            ok = wait_count(a1.dep + t.g, 2 * (s_off1[t.g + 1] - s_off1[t.g]), abort);
+            fence_proxy_async_global();
           }
-          const int stage = fills % kStages;
-          if (!mbar_wait<true>(&empty_bar[stage], ((fills / kStages) & 1) ^ 1u, abort)) {
-            flag_timeout(a.status, abort);
-            ok = false;
-            break;
-          }
-          if (lead) mbar_arrive_expect_tx(&full_bar[stage], tx_bytes);
-          const int kc = kb * kBK;
-          const uint32_t fb = lead_full + 8u * stage;
-          uint8_t* xs = sX + stage * kXStageBytes;
-          uint8_t* wsm = sW + stage * kWStageBytes;
-          if (t.token_major) {
-            tma_load_2d_pair(xs, &map_x128, fb, kc, xrow);
-            const int wrow = kFc1 ? (lead ? t.n0 : t.N + t.n0) : (t.n0 + 128 * r);
-            tma_load_3d_pair(wsm, mw128, fb, kc, wrow, ecoord);
-          } else {
-            for (int q = 0; q < half; q += 8)
-              tma_load_2d_pair(xs + q * kRowBytes, &map_x8, fb, kc, xrow + q);
-            if (kFc1) {
-              tma_load_3d_pair(wsm, mw64, fb, kc, t.n0 + 64 * r, ecoord);
-              tma_load_3d_pair(wsm + 64 * kRowBytes, mw64, fb, kc, t.N + t.n0 + 64 * r, ecoord);
-            } else {
-              tma_load_3d_pair(wsm, mw128, fb, kc, t.n0 + 128 * r, ecoord);
-            }
-          }
-          ++fills;
+          if (ok)
+            ok = pair_produce<false>(t, m2, a2, rank, lead, a1.sched, claimed, have_claim,
+                                     fills, sX, sW, lead_full, full_bar, empty_bar, abort);
         }
+        if (!ok) flag_timeout(a1.status, abort);
       }
       // Before this CTA may exit, the first CTA's commits for every stage it filled must
       // have arrived (they target this CTA's barriers); bounded.
@@ -1133,16 +1203,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
       for (int it = 0; ok; ++it) {
         const int slot = it & (kSchedDepth - 1);
         if (!mbar_wait<true>(&sched_full[slot], (it / kSchedDepth) & 1, abort)) {
-          flag_timeout(a.status, abort);
+          flag_timeout(a1.status, abort);
           ok = false;
           break;
         }
         const int unit = *reinterpret_cast<volatile int*>(&s_tile[slot]);
         release_slot(slot);
         if (unit < 0) break;
-        const Unit t = decode_unit(unit, s_off, s_cnt, s_start, a, kFc1, 0);
+        const Unit t = decode(unit, is_fc1(unit), 0u);
         if (!mbar_wait<true>(&tempty_bar[acc], acc_phase ^ 1u, abort)) {
-          flag_timeout(a.status, abort);
+          flag_timeout(a1.status, abort);
           ok = false;
           break;
         }
@@ -1155,7 +1225,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
                  : pair_k_loop<false>(d, idesc_bf16_f32(256, t.ntok), nkb, cons, sx0, sw0,
                                       full_bar, empty_bar, abort);
         if (!ok) {
-          flag_timeout(a.status, abort);
+          flag_timeout(a1.status, abort);
           break;
         }
         umma_commit_pair(&tfull_bar[acc], kPairMask);
@@ -1174,7 +1244,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
   } else {
     // -------------------------------------------------------------- epilogue (both CTAs)
     const int q = warp & 3;                 // TMEM lane quarter of this warp
-    const int lrow = q * 32 + lane;         // accumulator row (lane) of this thread
     uint8_t* my_out = sOut + q * 2 * kStoreBufBytes;
     int sbuf = 0;
     int acc = 0;
@@ -1183,34 +1252,43 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
       const int slot = it & (kSchedDepth - 1);
       const bool have = mbar_wait<true>(&sched_full[slot], (it / kSchedDepth) & 1, abort);
       if (!__all_sync(0xffffffffu, have)) {
-        flag_timeout(a.status, abort);
+        flag_timeout(a1.status, abort);
         break;
       }
       const int unit = *reinterpret_cast<volatile int*>(&s_tile[slot]);
       __syncwarp();
       if (lane == 0) release_slot(slot);
       if (unit < 0) break;
-      const Unit t = decode_unit(unit, s_off, s_cnt, s_start, a, kFc1, rank);
+      const bool fc1 = is_fc1(unit);
+      const Unit t = decode(unit, fc1, rank);
       const bool got = mbar_wait<true>(&tfull_bar[acc], acc_phase, abort);
       // Lanes may leave the poll at different times; tcgen05.ld is warp-collective.
       if (!__all_sync(0xffffffffu, got)) {
-        flag_timeout(a.status, abort);
+        flag_timeout(a1.status, abort);
         break;
       }
       tc_fence_after();
       const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * kAccCols) +
                           (static_cast<uint32_t>(q * 32) << 16);
-      if (t.token_major && t.rows == kTileRows)
-        store_token_major_tma<kFc1>(tb, t, q, lane, my_out, sbuf, &map_out);
-      else if (t.token_major)
-        store_token_major<kFc1>(tb, t, lrow, a);
-      else
-        store_weight_major<kFc1>(tb, t, lrow, rank, s_xchg, a);
+      if (fc1) pair_epilogue<true>(tb, t, q, lane, rank, my_out, sbuf, s_xchg, m1, a1);
+      else pair_epilogue<false>(tb, t, q, lane, rank, my_out, sbuf, s_xchg, m2, a2);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         if (lead) mbar_arrive(&tempty_bar[acc]);
         else mbar_arrive_cluster(lead_tempty + 8u * acc);
+      }
+      if (kFused && fc1) {
+        // Publish this CTA's h rows of the unit to the FC2 units of its group: every
+        // store of the four warps complete and visible (TMA stores: waited for, then a
+        // proxy fence), then one release add on the group's counter.
+        if (lane == 0) {
+          bulk_wait_group<0>();
+          fence_proxy_async_global();
+        }
+        __threadfence();
+        named_barrier_sync(2, 128);
+        if (q == 0 && lane == 0) red_release_gpu_add(a1.dep + t.g, 1);
       }
       if (++acc == 2) {
         acc = 0;
@@ -1229,7 +1307,43 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,  // A row
   }
   // No CTA leaves while the other may still write into it or arrive on its barriers.
   cluster_sync();
-  if (threadIdx.x == 0) finish_claims(a);
+  if (threadIdx.x == 0) finish_claims(a1);
+}
+
+template <bool kFc1>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,
+                         const __grid_constant__ CUtensorMap map_x8,
+                         const __grid_constant__ CUtensorMap map_w128,
+                         const __grid_constant__ CUtensorMap map_ws128,
+                         const __grid_constant__ CUtensorMap map_w64,
+                         const __grid_constant__ CUtensorMap map_ws64,
+                         const __grid_constant__ CUtensorMap map_out, GemmArgs a) {
+  const PairMaps m{&map_x128, &map_x8, &map_w128, &map_ws128, &map_w64, &map_ws64, &map_out};
+  pair_kernel_body<kFc1 ? kModeFc1 : kModeFc2>(m, m, a, a);
+}
+
+// Both GEMMs in one launch (FC1's units, then FC2's): maps and arguments of FC1 (x_perm,
+// w13, h) then of FC2 (h, w2, out_perm).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+grouped_gemm_pair_fused_kernel(const __grid_constant__ CUtensorMap f1_x128,
+                               const __grid_constant__ CUtensorMap f1_x8,
+                               const __grid_constant__ CUtensorMap f1_w128,
+                               const __grid_constant__ CUtensorMap f1_ws128,
+                               const __grid_constant__ CUtensorMap f1_w64,
+                               const __grid_constant__ CUtensorMap f1_ws64,
+                               const __grid_constant__ CUtensorMap f1_out,
+                               const __grid_constant__ CUtensorMap f2_x128,
+                               const __grid_constant__ CUtensorMap f2_x8,
+                               const __grid_constant__ CUtensorMap f2_w128,
+                               const __grid_constant__ CUtensorMap f2_ws128,
+                               const __grid_constant__ CUtensorMap f2_w64,
+                               const __grid_constant__ CUtensorMap f2_ws64,
+                               const __grid_constant__ CUtensorMap f2_out, GemmArgs a1,
+                               GemmArgs a2) {
+  const PairMaps m1{&f1_x128, &f1_x8, &f1_w128, &f1_ws128, &f1_w64, &f1_ws64, &f1_out};
+  const PairMaps m2{&f2_x128, &f2_x8, &f2_w128, &f2_ws128, &f2_w64, &f2_ws64, &f2_out};
+  pair_kernel_body<kModeFused>(m1, m2, a1, a2);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1254,6 +1368,9 @@ moe_status prepare_kernels(int* max_clusters) {
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSingleSmemBytes);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<kFc1>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess && kFc1)
+      e = cudaFuncSetAttribute(grouped_gemm_pair_fused_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess && kFc1)
       e = cudaFuncSetAttribute(grouped_gemm_fused_kernel<true>,
@@ -1431,12 +1548,24 @@ moe_status launch_fc12(const moe_problem& p, const moe_ws_layout& L, const void*
   moe_status st = setup_gemm<true>(p, L, w13, w13_s, e_lo, e_hi, ws, &g1);
   if (st == MOE_OK) st = setup_gemm<false>(p, L, w2, w2_s, e_lo, e_hi, ws, &g2);
   if (st != MOE_OK) return st;
-  if (g1.single_bound == 0 || g2.single_bound == 0) {
-    // CTA-pair sizes: two launches.
-    st = launch_gemm<true>(p, L, w13, w13_s, e_lo, e_hi, ws, s);
-    if (st == MOE_OK) st = launch_gemm<false>(p, L, w2, w2_s, e_lo, e_hi, ws, s);
-    return st;
+  if (g1.pair_bound > 0 && g2.pair_bound > 0) {
+    // CTA-pair sizes: one launch of the pair kernel for both GEMMs, as below.
+    GemmArgs a1 = g1.pair, a2 = g2.pair;
+    a1.dep = reinterpret_cast<int32_t*>(ws + L.sched) + kSchedCounters;
+    a2.dep = a1.dep;
+    a2.sched = a1.sched;
+    int64_t clusters = g1.max_clusters;
+    if (clusters > g1.pair_bound + g2.pair_bound) clusters = g1.pair_bound + g2.pair_bound;
+    const cudaError_t err = launch_pdl(
+        grouped_gemm_pair_fused_kernel, dim3(static_cast<unsigned>(2 * clusters)), dim3(kThreads),
+        kSmemBytes, s, g1.mx128, g1.mx8, g1.mw128, g1.mws128, g1.mw64, g1.mws64, g1.mout, g2.mx128,
+        g2.mx8, g2.mw128, g2.mws128, g2.mw64, g2.mws64, g2.mout, a1, a2);
+    if (err != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "grouped_gemm launch: %s", cudaGetErrorString(err));
+    return MOE_OK;
   }
+  if (g1.single_bound == 0 || g2.single_bound == 0)
+    return set_error(MOE_ERR_CUDA, "grouped_gemm: inconsistent launch bounds");
   // One persistent single-SM launch for both GEMMs: FC1's counter serves the joint list
   // and the per-group completion counters follow the work counters.
   GemmArgs a1 = g1.single, a2 = g2.single;
