@@ -9,6 +9,7 @@
  *   2. moe_permute   rows of x gathered into contiguous per-expert blocks
  *   3. moe_fc1       grouped GEMM x_perm . w13[e]^T with SwiGLU fused -> h
  *   4. moe_fc2       grouped GEMM h . w2[e]^T -> out_perm
+ *      (moe_fc1_fc2  steps 3 and 4 in one persistent launch, as moe_forward runs them)
  *   5. moe_finalize  unpermute, apply the routing weights, add the shared expert -> y
  *
  * moe_forward runs steps 2-5. Conventions common to every call:
@@ -256,6 +257,12 @@ moe_status moe_fc1(const moe_problem* p, const void* w13, const void* w13_s, voi
 /* Step 4: out_perm[r, :] = h[r] . w2[e]^T. */
 moe_status moe_fc2(const moe_problem* p, const void* w2, const void* w2_s, void* workspace,
                    size_t ws_bytes, void* stream);
+/* Steps 3 and 4 as moe_forward runs them: one persistent launch whose work list holds
+ * FC1's tiles, then FC2's; an FC2 tile starts once every FC1 tile of its expert has
+ * stored its h rows (a per-expert completion counter in the workspace, bounded wait).
+ * Same results, bit for bit, as moe_fc1 followed by moe_fc2. */
+moe_status moe_fc1_fc2(const moe_problem* p, const void* w13, const void* w13_s, const void* w2,
+                       const void* w2_s, void* workspace, size_t ws_bytes, void* stream);
 /* Step 5 (TensorRT-LLM MoE page: routing weights applied after FC2; finalize = top-k
  * weighted row sum): y[t] = sum_j scales[t,j] * out_perm[perm_inv[t*k+j]] (+ shared row). */
 moe_status moe_finalize(const moe_problem* p, const float* scales, void* y, void* workspace,

@@ -77,6 +77,8 @@ _SIGS = {
     "moe_permute": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_fc1": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_fc2": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_fc1_fc2": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, _P, _P, ctypes.c_size_t,
+                                   _P]),
     "moe_finalize": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_read_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "moe_selftest_wait": (ctypes.c_int, [_P, _P]),
@@ -317,6 +319,11 @@ def moe_fc1(problem, w13, w13_s, workspace: Workspace, stream=None):
 def moe_fc2(problem, w2, w2_s, workspace: Workspace, stream=None):
     _check(_lib.moe_fc2(ctypes.byref(problem), _ptr(w2), _ptr(w2_s), workspace.ptr,
                         workspace.nbytes, _stream(stream)), "moe_fc2")
+
+
+def moe_fc1_fc2(problem, w13, w13_s, w2, w2_s, workspace: Workspace, stream=None):
+    _check(_lib.moe_fc1_fc2(ctypes.byref(problem), _ptr(w13), _ptr(w13_s), _ptr(w2), _ptr(w2_s),
+                            workspace.ptr, workspace.nbytes, _stream(stream)), "moe_fc1_fc2")
 
 
 def moe_finalize(problem, scales, y, workspace: Workspace, stream=None):

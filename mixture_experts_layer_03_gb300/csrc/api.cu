@@ -231,6 +231,19 @@ moe_status moe_fc2(const moe_problem* p, const void* w2, const void* w2_s, void*
                     static_cast<cudaStream_t>(stream));
 }
 
+moe_status moe_fc1_fc2(const moe_problem* p, const void* w13, const void* w13_s, const void* w2,
+                       const void* w2_s, void* workspace, size_t ws_bytes, void* stream) {
+  moe_ws_layout L;
+  moe_status st = check_forward_common(p, workspace, ws_bytes, &L);
+  if (st != MOE_OK || p->T == 0) return st;
+  if (!w13 || !aligned16(w13) || !w2 || !aligned16(w2))
+    return set_error(MOE_ERR_INVALID_ARG, "w13/w2 NULL or not 16-byte aligned");
+  if (!shared_args_ok(p, w13_s, w2_s))
+    return set_error(MOE_ERR_INVALID_ARG, "shared expert weights NULL or not 16-byte aligned");
+  return launch_fc12(*p, L, w13, w13_s, w2, w2_s, 0, p->E, static_cast<char*>(workspace),
+                     static_cast<cudaStream_t>(stream));
+}
+
 moe_status moe_finalize(const moe_problem* p, const float* scales, void* y, void* workspace,
                         size_t ws_bytes, void* stream) {
   moe_ws_layout L;

@@ -33,7 +33,8 @@ def _declared_functions():
 
 def test_header_declares_the_step_calls():
     names = _declared_functions()
-    for n in ("moe_route", "moe_forward", "moe_permute", "moe_fc1", "moe_fc2", "moe_finalize",
+    for n in ("moe_route", "moe_forward", "moe_permute", "moe_fc1", "moe_fc2", "moe_fc1_fc2",
+              "moe_finalize",
               "moe_can_implement", "moe_workspace_bytes", "moe_read_device_status"):
         assert n in names
 

@@ -253,6 +253,22 @@ def test_forward_steps_parity(moe, case):
         _check_close(h[P:, :sI], hs_ref, H_TOL, "shared FC1")
         _check_close(out[P:], hs_ref @ w2s.T, Y_TOL, "shared FC2")
     _check_close(y.cpu().double().numpy(), y_ref, Y_TOL, "y")
+    # FC1 and FC2 in one launch (moe_fc1_fc2, the launch moe_forward runs) write the same
+    # h and out_perm bytes as the two separate launches
+    h_steps = ws.region("h", R * Ih, torch.bfloat16).clone()
+    out_steps = ws.region("out_perm", R * H, torch.bfloat16).clone()
+    ws.region("h", R * Ih, torch.bfloat16).fill_(float("nan"))
+    ws.region("out_perm", R * H, torch.bfloat16).fill_(float("nan"))
+    moe.moe_permute(p, dev["x"], dev["ids"], ws)
+    moe.moe_fc1_fc2(p, dev["w13"], dev["w13s"], dev["w2"], dev["w2s"], ws)
+    torch.cuda.synchronize()
+    h_f = ws.region("h", R * Ih, torch.bfloat16).view(R, Ih)
+    h_s = h_steps.view(R, Ih)
+    assert torch.equal(h_f[:P, :I].view(torch.int16), h_s[:P, :I].view(torch.int16))
+    if sI:
+        assert torch.equal(h_f[P:, :sI].view(torch.int16), h_s[P:, :sI].view(torch.int16))
+    assert torch.equal(ws.region("out_perm", R * H, torch.bfloat16).view(torch.int16),
+                       out_steps.view(torch.int16))
     # moe_forward (one call) gives the same bytes as the four steps
     y2 = moe.moe_forward(dev["x"], dev["ids"], dev["sc"], dev["w13"], dev["w2"], dev["w13s"],
                          dev["w2s"], workspace=ws)
