@@ -1,26 +1,26 @@
-// Steps 3 and 4: grouped GEMM over all experts, two persistent launches per GEMM.
-//
+// Steps 3 and 4: grouped GEMM over all experts; the forward runs both as ONE persistent
+// launch (FC1's work list, then FC2's; an FC2 tile of expert g waits on a counter for
+// g's FC1 tiles), and moe_fc1 / moe_fc2 run one GEMM each with the same tiles.
 // Scheduling (Dense GEMM -> GroupedGEMM article, section 2.2): tile scheduling over
 // flattened global work lists rather than one block per expert. The permute step wrote,
 // per group g (routed experts, then the optional shared expert), its row count m_g, its
-// first permuted row and exclusive scans of its work. Each group goes to ONE kernel, so
-// the units that share a weight panel run close together in time and reuse it in L2:
-//
-//  * groups with m_g >= 256 -> grouped_gemm_pair_kernel, on 2-CTA clusters with pair
-//    MMAs (tcgen05.mma.cta_group::2, M = 256). Each CTA holds 128 rows of the A operand
-//    and half of the B operand in its own shared memory, so a stage is 32 KB per SM and
-//    six stages fit; each CTA's TMEM receives its 128 rows of the result. A group gives
-//    floor(m_g / 256) token-major units (two full 128-row tiles, one per CTA,
+// first permuted row and exclusive scans of its work. One kernel family takes every group
+// of a launch: the CTA-pair kernel when T*k >= 256*E, else the single-SM kernel.
+//  * CTA-pair kernel: 2-CTA clusters with pair MMAs (tcgen05.mma.cta_group::2, M = 256).
+//    Each CTA holds 128 rows of the A operand and half of the B operand in its own shared
+//    memory, so a stage is 32 KB per SM and six stages fit; each CTA's TMEM receives its
+//    128 rows of the result. A group gives floor(m_g / 256) token-major units (two full
+//    128-row tiles, one per CTA,
 //        D[256 tokens, 256] = X[256, K] . W[256, K]^T,   A = X, B = W, N = 256)
 //    and one unit for the rows left over: 129..255 rows run token-major with the
 //    missing rows masked; 1..128 rows run weight-major (swap AB,
 //        D[256 weights, n] = W[256, K] . X[n, K]^T,      A = W, B = X,
 //    n = rows rounded up to 16, each CTA holding n/2 token rows), per channel tile.
-//  * groups with m_g < 256 (every decode-sized expert) -> grouped_gemm_kernel, one SM per
-//    tile: a full 128-row tile token-major (D[128, 256] = X . W^T, N = 256) and the
-//    partial tile weight-major (D0[128 ch, n] = W[0:128] . X^T, D1 = W[128:256] . X^T, with
-//    n = rows rounded up to 16); 48 KB stages keep 32 KB of weights per stage in flight,
-//    which is what a weight-streaming (HBM-bound) tile needs.
+//  * single-SM kernel (decode-sized experts), one SM per tile: a full 128-row tile
+//    token-major (D[128, 256] = X . W^T, N = 256) and the partial tile weight-major
+//    (D0[128 ch, n] = W[0:128] . X^T, D1 = W[128:256] . X^T, n = rows rounded up to 16);
+//    48 KB stages keep 32 KB of weights per stage in flight, which is what a
+//    weight-streaming (HBM-bound) tile needs.
 //
 // Weight rows (w13 = gate and up merged, vLLM MoE page, section "专家权重如何存储") are
 // arranged so the SwiGLU epilogue (h = silu(gate) * up) finds gate and up of a channel in
