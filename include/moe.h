@@ -260,7 +260,8 @@ moe_status moe_fc2(const moe_problem* p, const void* w2, const void* w2_s, void*
 /* Steps 3 and 4 as moe_forward runs them: one persistent launch whose work list holds
  * FC1's tiles, then FC2's; an FC2 tile starts once every FC1 tile of its expert has
  * stored its h rows (a per-expert completion counter in the workspace, bounded wait).
- * Same results, bit for bit, as moe_fc1 followed by moe_fc2. */
+ * Same results, bit for bit, as moe_fc1 followed by moe_fc2. Call it after moe_permute on
+ * the same workspace: that step zeroes the counters it uses. */
 moe_status moe_fc1_fc2(const moe_problem* p, const void* w13, const void* w13_s, const void* w2,
                        const void* w2_s, void* workspace, size_t ws_bytes, void* stream);
 /* Step 5 (TensorRT-LLM MoE page: routing weights applied after FC2; finalize = top-k
