@@ -11,7 +11,11 @@
 //                  keep ascending flat index f = t*k + j. Chunk 0 also writes counts,
 //                  starts, offsets and the FC1/FC2 tile lists.
 //   gather_kernel  x_perm[r] = x[perm_src[r] / k] (and x[t] for the shared rows),
-//                  16-byte vector copies, one warp per row.
+//                  16-byte vector copies, one warp per row (decode-sized batches).
+//   scatter_kernel the same rows, token-major: one warp per token reads x[t] once and
+//                  writes it to each of its permuted rows perm_inv[t*k + j] (and the
+//                  shared row). With many tokens, x is then read from HBM once instead
+//                  of once per slot through L2 (batches of at least kScatterMinTokens).
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -23,6 +27,9 @@ namespace moe {
 namespace {
 
 constexpr int kPermWarps = kPermThreads / 32;
+// Batches with at least this many tokens copy rows token-major (scatter_kernel): enough
+// warps (one per token) to keep every SM busy. Smaller batches copy row by row.
+constexpr int64_t kScatterMinTokens = 2048;
 
 __global__ void __launch_bounds__(kPermThreads)
 hist_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int e_lo, int e_hi,
@@ -284,6 +291,51 @@ gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ p
   }
 }
 
+// Token-major row copy (see the header): warp w takes tokens w, w + warps, ...; lane j < k
+// reads perm_inv[t*k + j] and every lane gets all k destination rows by shuffles. Each
+// 16-byte vector of x[t] is loaded once and stored to every destination (streaming
+// stores). Slots whose id was invalid or belongs to another call (perm_inv = -1) write
+// nothing.
+__global__ void __launch_bounds__(256)
+scatter_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ perm_inv,
+               int64_t T, int k, int64_t P, int has_shared, int H,
+               __nv_bfloat16* __restrict__ x_perm) {
+  constexpr int kMaxDst = 9;   // up to 8 slots and the shared row
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  pdl_trigger();
+  pdl_wait();
+  const int nvec = H / 8;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       t < T; t += warps) {
+    const int32_t mine = lane < k ? perm_inv[t * k + lane] : -1;
+    int32_t dst[kMaxDst];   // permuted rows (< 2^31), -1 = none
+#pragma unroll
+    for (int j = 0; j < 8; ++j) dst[j] = __shfl_sync(0xffffffffu, mine, j);
+    dst[8] = has_shared ? static_cast<int32_t>(P + t) : -1;
+    const uint4* s = reinterpret_cast<const uint4*>(x + t * H);
+    int v = lane;
+    for (; v + 224 < nvec; v += 256) {
+      uint4 a[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) a[q] = __ldg(s + v + 32 * q);
+#pragma unroll
+      for (int j = 0; j < kMaxDst; ++j) {
+        if (dst[j] < 0) continue;
+        uint4* d = reinterpret_cast<uint4*>(x_perm + static_cast<int64_t>(dst[j]) * H);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) __stcs(d + v + 32 * q, a[q]);
+      }
+    }
+    for (; v < nvec; v += 32) {
+      const uint4 a = __ldg(s + v);
+#pragma unroll
+      for (int j = 0; j < kMaxDst; ++j)
+        if (dst[j] >= 0) __stcs(reinterpret_cast<uint4*>(x_perm + static_cast<int64_t>(dst[j]) * H) + v, a);
+    }
+  }
+}
+
 }  // namespace
 
 moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const void* x,
@@ -325,13 +377,22 @@ moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const vo
   }
   if (err == cudaSuccess) {
     const int sms = device_sm_count();
-    const int64_t rows = L.rows;
-    int64_t blocks = (rows + 7) / 8;
-    if (blocks > static_cast<int64_t>(sms) * 16) blocks = static_cast<int64_t>(sms) * 16;
-    err = launch_pdl(gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
-                     static_cast<const __nv_bfloat16*>(x), static_cast<const int32_t*>(a.perm_src),
-                     static_cast<const int32_t*>(a.offsets), P, p.E, p.k, rows, p.H,
-                     reinterpret_cast<__nv_bfloat16*>(ws + L.x_perm));
+    const int64_t cap = static_cast<int64_t>(sms) * 16;
+    if (p.T >= kScatterMinTokens) {
+      int64_t blocks = (p.T + 7) / 8;
+      if (blocks > cap) blocks = cap;
+      err = launch_pdl(scatter_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                       static_cast<const __nv_bfloat16*>(x), static_cast<const int32_t*>(a.perm_inv),
+                       p.T, p.k, P, a.has_shared, p.H, reinterpret_cast<__nv_bfloat16*>(ws + L.x_perm));
+    } else {
+      const int64_t rows = L.rows;
+      int64_t blocks = (rows + 7) / 8;
+      if (blocks > cap) blocks = cap;
+      err = launch_pdl(gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                       static_cast<const __nv_bfloat16*>(x), static_cast<const int32_t*>(a.perm_src),
+                       static_cast<const int32_t*>(a.offsets), P, p.E, p.k, rows, p.H,
+                       reinterpret_cast<__nv_bfloat16*>(ws + L.x_perm));
+    }
   }
   if (err != cudaSuccess) return set_error(MOE_ERR_CUDA, "permute launch: %s", cudaGetErrorString(err));
   return MOE_OK;

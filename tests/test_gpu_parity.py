@@ -166,6 +166,36 @@ def test_permute_parity(moe, T, E, k):
 
 # ------------------------------------------------------------------------ forward (small)
 
+@pytest.mark.parametrize("T", [300, 2500])   # row-by-row copy below 2048 tokens, token-major at and above
+def test_permute_rows_with_shared_expert_and_invalid_ids(moe, T):
+    """x_perm byte for byte with a shared expert (its rows P + t hold x[t]) and two slots
+    whose ids are out of range (no row, perm_inv = -1, status flagged), in both row-copy
+    forms of the permute step."""
+    E, k, H, I, sI = 16, 4, 256, 128, 128
+    g = torch.Generator().manual_seed(T)
+    ids = torch.randint(0, E, (T, k), generator=g, dtype=torch.int32)
+    ids[5, 1] = E
+    ids[T - 1, 0] = -3
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    p = moe.make_problem(T, H, I, E, k, sI)
+    ws = moe.alloc_workspace(p)
+    moe.moe_permute(p, x.cuda(), ids.cuda(), ws)
+    torch.cuda.synchronize()
+    flat = ids.numpy().reshape(-1)
+    valid = (flat >= 0) & (flat < E)
+    # Invalid slots as a sentinel expert E that sorts after every real one: the first n
+    # rows of the oracle's permutation are then the valid rows in their stable order.
+    _, _, perm_src, _ = oracle.permute(np.where(valid, flat, E).reshape(T, k), E + 1)
+    n, P = int(valid.sum()), T * k
+    xp = ws.region("x_perm", (P + T) * H, torch.bfloat16).view(P + T, H).cpu()
+    assert torch.equal(xp[:n], x[torch.from_numpy(perm_src[:n]).long() // k])
+    assert torch.equal(xp[P:], x)
+    pinv = ws.region("perm_inv", P, torch.int32).cpu().numpy()
+    assert pinv[5 * k + 1] == -1 and pinv[(T - 1) * k] == -1
+    st, flags = moe.moe_read_device_status(ws)
+    assert st == moe.MOE_ERR_DEVICE_BAD_ID and flags & moe.MOE_DEVICE_FLAG_BAD_ID
+
+
 def _random_case(T, H, I, E, k, shared_I=0, seed=0, ids_mode="route", method=RENORMALIZE_NAIVE):
     g = torch.Generator().manual_seed(seed)
     logits = torch.randn(T, E, generator=g)
