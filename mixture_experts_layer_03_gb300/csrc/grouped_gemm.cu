@@ -128,6 +128,22 @@ __device__ __forceinline__ int find_group(int idx, const int32_t* s_off, int G) 
   return lo;
 }
 
+// FC2 work of group g in the fused launch reads the h rows its FC1 tiles stored: the
+// producer waits (acquire, bounded) until the group's completion counter shows them all,
+// then fences the async proxy for its TMA loads. A group's h rows never change after that,
+// so each producer remembers the groups it has seen complete (one bit per group in shared
+// memory, touched by the producer thread only) and skips the global load for them.
+constexpr int kDepWords = (kMaxGroups + 31) / 32;
+__device__ __forceinline__ bool wait_group_h(uint32_t* seen, const int32_t* dep, int g, int need,
+                                             volatile int* abort) {
+  const uint32_t bit = 1u << (g & 31);
+  if (seen[g >> 5] & bit) return true;
+  if (!wait_count(dep + g, need, abort)) return false;
+  fence_proxy_async_global();
+  seen[g >> 5] |= bit;
+  return true;
+}
+
 __device__ __forceinline__ Unit decode_unit(int unit, const int32_t* s_off, const int32_t* s_cnt,
                                             const int32_t* s_start, const GemmArgs& a, bool fc1,
                                             uint32_t rank) {
@@ -596,6 +612,7 @@ __device__ __forceinline__ void single_kernel_body(const SingleMaps& m1, const S
   __shared__ int32_t s_off1[kMode == kModeFc2 ? 1 : kMaxGroups + 1];
   __shared__ int32_t s_off2[kMode == kModeFc1 ? 1 : kMaxGroups + 1];
   __shared__ int32_t s_cnt[kMaxGroups], s_start[kMaxGroups];
+  __shared__ uint32_t s_dep_seen[kDepWords];
   constexpr bool kFused = kMode == kModeFused;
 
   const int warp = threadIdx.x >> 5;
@@ -623,6 +640,7 @@ __device__ __forceinline__ void single_kernel_body(const SingleMaps& m1, const S
       mbar_init(&sched_full[s], 1);
       mbar_init(&sched_empty[s], 1 + 4);   // the MMA thread + one arrival per epilogue warp
     }
+    for (int i = 0; i < kDepWords; ++i) s_dep_seen[i] = 0;
     s_abort = 0;
     fence_barrier_init();
   }
@@ -721,10 +739,8 @@ __device__ __forceinline__ void single_kernel_body(const SingleMaps& m1, const S
                                              empty_bar, abort);
         } else {
           if (kFused) {
-            // h rows of group g are complete once all its FC1 tiles have signalled; the
-            // TMA loads that follow read them through the async proxy.
-            ok = wait_count(a1.dep + t.g, s_off1[t.g + 1] - s_off1[t.g], abort);
-            fence_proxy_async_global();
+            // h rows of group g are complete once all its FC1 tiles have signalled.
+            ok = wait_group_h(s_dep_seen, a1.dep, t.g, s_off1[t.g + 1] - s_off1[t.g], abort);
           }
           if (ok)
             ok = single_produce<false, kNarrow>(t, m2, a2, stage, phase, issued, sX, sW,
@@ -1044,6 +1060,7 @@ __device__ __forceinline__ void pair_kernel_body(const PairMaps& m1, const PairM
   __shared__ int32_t s_off2[kMode == kModeFc1 ? 1 : kMaxGroups + 1];
   __shared__ int32_t s_cnt[kMaxGroups], s_start[kMaxGroups];
   __shared__ float s_xchg[64 * kXchgStride];
+  __shared__ uint32_t s_dep_seen[kDepWords];
   constexpr bool kFused = kMode == kModeFused;
 
   const int warp = threadIdx.x >> 5;
@@ -1076,6 +1093,7 @@ __device__ __forceinline__ void pair_kernel_body(const PairMaps& m1, const PairM
       mbar_init(&sched_full[s], 1);
       mbar_init(&sched_empty[s], kSchedConsumers);   // used in the first CTA only
     }
+    for (int i = 0; i < kDepWords; ++i) s_dep_seen[i] = 0;
     s_abort = 0;
     fence_barrier_init();
   }
@@ -1174,10 +1192,9 @@ __device__ __forceinline__ void pair_kernel_body(const PairMaps& m1, const PairM
                                   sX, sW, lead_full, full_bar, empty_bar, abort);
         } else {
           if (kFused) {
-            // Both CTAs of every FC1 unit of group g signal once their h rows are stored;
-            // the TMA loads that follow read those rows through the async proxy.
-            ok = wait_count(a1.dep + t.g, 2 * (s_off1[t.g + 1] - s_off1[t.g]), abort);
-            fence_proxy_async_global();
+            // Both CTAs of every FC1 unit of group g signal once their h rows are stored.
+            ok = wait_group_h(s_dep_seen, a1.dep, t.g, 2 * (s_off1[t.g + 1] - s_off1[t.g]),
+                              abort);
           }
           if (ok)
             ok = pair_produce<false>(t, m2, a2, rank, lead, a1.sched, claimed, have_claim,
