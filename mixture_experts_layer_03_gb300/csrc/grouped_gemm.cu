@@ -962,7 +962,7 @@ __device__ __forceinline__ bool pair_k_loop(uint32_t d, uint32_t idesc, int nkb,
 // parameters.
 struct PairMaps {
   const CUtensorMap* x128;   // A rows, box 64 x 128
-  const CUtensorMap* x8;     // A rows, box 64 x 8
+  const CUtensorMap* x64;    // A rows, box 64 x 64
   const CUtensorMap* w128;   // routed weights, box 64 x 128
   const CUtensorMap* ws128;  // shared weights, box 64 x 128
   const CUtensorMap* w64;    // routed weights, box 64 x 64
@@ -988,9 +988,10 @@ __device__ __forceinline__ bool pair_produce(const Unit& t, const PairMaps& m, c
   // This CTA's token rows and its share of the weight rows.
   const int half = t.ntok >> 1;
   const int xrow = t.token_major ? t.row0 : t.row0 + r * half;
-  // Weight-major units have at most 128 token rows: each CTA loads its <= 64 rows in
-  // 8-row boxes (the same byte count in both CTAs).
-  const uint32_t xbytes = t.token_major ? kXStageBytes : static_cast<uint32_t>(half) * kRowBytes;
+  // Weight-major units have at most 128 token rows: each CTA loads its <= 64 rows as one
+  // 64-row box (rows past its share land in the stage but the MMA, N = ntok, never reads
+  // them; rows past the tensor are zero-filled).
+  const uint32_t xbytes = t.token_major ? kXStageBytes : 64u * kRowBytes;
   const uint32_t tx_bytes = 2u * (xbytes + kWStageBytes);
   const int nkb = t.K / kBK;
   const int claim_kb = nkb > kClaimLead ? nkb - kClaimLead : 0;
@@ -1011,8 +1012,7 @@ __device__ __forceinline__ bool pair_produce(const Unit& t, const PairMaps& m, c
       const int wrow = kFc1 ? (lead ? t.n0 : t.N + t.n0) : (t.n0 + 128 * r);
       tma_load_3d_pair(wsm, mw128, fb, kc, wrow, ecoord);
     } else {
-      for (int q = 0; q < half; q += 8)
-        tma_load_2d_pair(xs + q * kRowBytes, m.x8, fb, kc, xrow + q);
+      tma_load_2d_pair(xs, m.x64, fb, kc, xrow);
       if (kFc1) {
         tma_load_3d_pair(wsm, mw64, fb, kc, t.n0 + 64 * r, ecoord);
         tma_load_3d_pair(wsm + 64 * kRowBytes, mw64, fb, kc, t.N + t.n0 + 64 * r, ecoord);
@@ -1101,7 +1101,7 @@ __device__ __forceinline__ void pair_kernel_body(const PairMaps& m1, const PairM
     const PairMaps* ms[2] = {&m1, &m2};
     for (int i = (kMode == kModeFc2 ? 1 : 0); i < (kMode == kModeFc1 ? 1 : 2); ++i) {
       tma_prefetch_map(ms[i]->x128);
-      tma_prefetch_map(ms[i]->x8);
+      tma_prefetch_map(ms[i]->x64);
       tma_prefetch_map(ms[i]->w128);
       tma_prefetch_map(ms[i]->ws128);
       tma_prefetch_map(ms[i]->w64);
@@ -1330,13 +1330,13 @@ __device__ __forceinline__ void pair_kernel_body(const PairMaps& m1, const PairM
 template <bool kFc1>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,
-                         const __grid_constant__ CUtensorMap map_x8,
+                         const __grid_constant__ CUtensorMap map_x64,
                          const __grid_constant__ CUtensorMap map_w128,
                          const __grid_constant__ CUtensorMap map_ws128,
                          const __grid_constant__ CUtensorMap map_w64,
                          const __grid_constant__ CUtensorMap map_ws64,
                          const __grid_constant__ CUtensorMap map_out, GemmArgs a) {
-  const PairMaps m{&map_x128, &map_x8, &map_w128, &map_ws128, &map_w64, &map_ws64, &map_out};
+  const PairMaps m{&map_x128, &map_x64, &map_w128, &map_ws128, &map_w64, &map_ws64, &map_out};
   pair_kernel_body<kFc1 ? kModeFc1 : kModeFc2>(m, m, a, a);
 }
 
@@ -1344,22 +1344,22 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_x128,
 // w13, h) then of FC2 (h, w2, out_perm).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 grouped_gemm_pair_fused_kernel(const __grid_constant__ CUtensorMap f1_x128,
-                               const __grid_constant__ CUtensorMap f1_x8,
+                               const __grid_constant__ CUtensorMap f1_x64,
                                const __grid_constant__ CUtensorMap f1_w128,
                                const __grid_constant__ CUtensorMap f1_ws128,
                                const __grid_constant__ CUtensorMap f1_w64,
                                const __grid_constant__ CUtensorMap f1_ws64,
                                const __grid_constant__ CUtensorMap f1_out,
                                const __grid_constant__ CUtensorMap f2_x128,
-                               const __grid_constant__ CUtensorMap f2_x8,
+                               const __grid_constant__ CUtensorMap f2_x64,
                                const __grid_constant__ CUtensorMap f2_w128,
                                const __grid_constant__ CUtensorMap f2_ws128,
                                const __grid_constant__ CUtensorMap f2_w64,
                                const __grid_constant__ CUtensorMap f2_ws64,
                                const __grid_constant__ CUtensorMap f2_out, GemmArgs a1,
                                GemmArgs a2) {
-  const PairMaps m1{&f1_x128, &f1_x8, &f1_w128, &f1_ws128, &f1_w64, &f1_ws64, &f1_out};
-  const PairMaps m2{&f2_x128, &f2_x8, &f2_w128, &f2_ws128, &f2_w64, &f2_ws64, &f2_out};
+  const PairMaps m1{&f1_x128, &f1_x64, &f1_w128, &f1_ws128, &f1_w64, &f1_ws64, &f1_out};
+  const PairMaps m2{&f2_x128, &f2_x64, &f2_w128, &f2_ws128, &f2_w64, &f2_ws64, &f2_out};
   pair_kernel_body<kModeFused>(m1, m2, a1, a2);
 }
 
@@ -1417,7 +1417,7 @@ moe_status prepare_kernels(int* max_clusters) {
 
 // The tensor maps, arguments and work bounds of one GEMM.
 struct GemmSetup {
-  CUtensorMap mx128, mx8, mx16, mw128, mws128, mw64, mws64, mout;
+  CUtensorMap mx128, mx64, mx16, mw128, mws128, mw64, mws64, mout;
   GemmArgs pair, single;        // arguments of the pair and single-SM launches
   int64_t pair_bound, single_bound;
   bool narrow;
@@ -1434,7 +1434,7 @@ moe_status setup_gemm(const moe_problem& p, const moe_ws_layout& L, const void* 
   const int has_shared = p.shared_I > 0;
   const void* A = kFc1 ? static_cast<const void*>(ws + L.x_perm) : static_cast<const void*>(ws + L.h);
   const uint64_t a_cols = kFc1 ? static_cast<uint64_t>(p.H) : static_cast<uint64_t>(L.h_ld);
-  bool ok = encode_map2(&g->mx128, A, R, a_cols, 128) && encode_map2(&g->mx8, A, R, a_cols, 8) &&
+  bool ok = encode_map2(&g->mx128, A, R, a_cols, 128) && encode_map2(&g->mx64, A, R, a_cols, 64) &&
             encode_map2(&g->mx16, A, R, a_cols, 16);
   // Weights [planes, rows, K]: FC1 w13 [E, 2I, H] (shared [1, 2Is, H]); FC2 w2 [E, H, I]
   // (shared [1, H, Is]).
@@ -1538,7 +1538,7 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
     int64_t clusters = g.max_clusters;
     if (clusters > g.pair_bound) clusters = g.pair_bound;
     err = launch_pdl(grouped_gemm_pair_kernel<kFc1>, dim3(static_cast<unsigned>(2 * clusters)),
-                     dim3(kThreads), kSmemBytes, s, g.mx128, g.mx8, g.mw128, g.mws128, g.mw64,
+                     dim3(kThreads), kSmemBytes, s, g.mx128, g.mx64, g.mw128, g.mws128, g.mw64,
                      g.mws64, g.mout, g.pair);
   }
   if (err != cudaSuccess)
@@ -1575,8 +1575,8 @@ moe_status launch_fc12(const moe_problem& p, const moe_ws_layout& L, const void*
     if (clusters > g1.pair_bound + g2.pair_bound) clusters = g1.pair_bound + g2.pair_bound;
     const cudaError_t err = launch_pdl(
         grouped_gemm_pair_fused_kernel, dim3(static_cast<unsigned>(2 * clusters)), dim3(kThreads),
-        kSmemBytes, s, g1.mx128, g1.mx8, g1.mw128, g1.mws128, g1.mw64, g1.mws64, g1.mout, g2.mx128,
-        g2.mx8, g2.mw128, g2.mws128, g2.mw64, g2.mws64, g2.mout, a1, a2);
+        kSmemBytes, s, g1.mx128, g1.mx64, g1.mw128, g1.mws128, g1.mw64, g1.mws64, g1.mout, g2.mx128,
+        g2.mx64, g2.mw128, g2.mws128, g2.mw64, g2.mws64, g2.mout, a1, a2);
     if (err != cudaSuccess)
       return set_error(MOE_ERR_CUDA, "grouped_gemm launch: %s", cudaGetErrorString(err));
     return MOE_OK;
