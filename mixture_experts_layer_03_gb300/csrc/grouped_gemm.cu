@@ -478,6 +478,7 @@ __device__ __forceinline__ bool single_k_loop_narrow(uint32_t d, uint32_t idesc,
 struct SingleMaps {
   const CUtensorMap* x128;   // A rows, box 64 x 128
   const CUtensorMap* x16;    // A rows, box 64 x 16
+  const CUtensorMap* x64;    // A rows, box 64 x 64
   const CUtensorMap* w;      // routed weights [planes, R, K], box 64 x 128
   const CUtensorMap* ws;     // shared weights [1, R, K]
   const CUtensorMap* w64;    // routed, box 64 x 64 (narrow launches only)
@@ -504,7 +505,12 @@ __device__ __forceinline__ bool single_produce(const Unit& t, const SingleMaps& 
   const int wr0 = t.n0;
   const int wr1 = kFc1 ? (t.N + t.n0) : (t.n0 + 128);
   const uint32_t xbytes = static_cast<uint32_t>(t.ntok) * kRowBytes;
-  const uint32_t bytes = (2 * kWStageBytes) + (t.token_major ? kXStageBytes : xbytes);
+  // A wide weight-major tile (a group's last partial tile) loads its X rows as at most two
+  // 16-row boxes, else as one 64- or 128-row box per stage (rows past ntok land in the
+  // stage; the MMA, N = ntok, never reads them; rows past the tensor are zero-filled).
+  const int xbox = t.ntok <= 32 ? 16 : (t.ntok <= 64 ? 64 : 128);
+  const uint32_t xwide = xbox == 16 ? xbytes : static_cast<uint32_t>(xbox) * kRowBytes;
+  const uint32_t bytes = (2 * kWStageBytes) + (t.token_major ? kXStageBytes : xwide);
   const int nkb = t.K / kBK;
   // Narrow tiles: two K blocks per stage; FC1 W blocks are 64 gate rows (64-row boxes)
   // then the 64 up rows, FC2 W blocks 128 channel rows.
@@ -533,8 +539,10 @@ __device__ __forceinline__ bool single_produce(const Unit& t, const SingleMaps& 
     } else {
       mbar_arrive_expect_tx(&full_bar[stage], bytes);
       const int kc = j * kBK;
-      if (t.token_major) {
+      if (t.token_major || xbox == 128) {
         tma_load_2d(xs, m.x128, &full_bar[stage], kc, t.row0);
+      } else if (xbox == 64) {
+        tma_load_2d(xs, m.x64, &full_bar[stage], kc, t.row0);
       } else {
         for (int r = 0; r < t.ntok; r += 16)
           tma_load_2d(xs + r * kRowBytes, m.x16, &full_bar[stage], kc, t.row0 + r);
@@ -648,6 +656,7 @@ __device__ __forceinline__ void single_kernel_body(const SingleMaps& m1, const S
     if (kMode != kModeFc2) {
       tma_prefetch_map(m1.x128);
       tma_prefetch_map(m1.x16);
+      tma_prefetch_map(m1.x64);
       tma_prefetch_map(m1.w);
       tma_prefetch_map(m1.ws);
       tma_prefetch_map(m1.out);
@@ -655,6 +664,7 @@ __device__ __forceinline__ void single_kernel_body(const SingleMaps& m1, const S
     if (kMode != kModeFc1) {
       tma_prefetch_map(m2.x128);
       tma_prefetch_map(m2.x16);
+      tma_prefetch_map(m2.x64);
       tma_prefetch_map(m2.w);
       tma_prefetch_map(m2.ws);
       tma_prefetch_map(m2.out);
@@ -884,9 +894,9 @@ __device__ __forceinline__ void single_kernel_body(const SingleMaps& m1, const S
 template <bool kFc1>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_x128, const __grid_constant__ CUtensorMap map_x16,
-                    const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_ws,
+                    const __grid_constant__ CUtensorMap map_x64, const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_ws,
                     const __grid_constant__ CUtensorMap map_out, GemmArgs a) {
-  const SingleMaps m{&map_x128, &map_x16, &map_w, &map_ws, nullptr, nullptr, &map_out};
+  const SingleMaps m{&map_x128, &map_x16, &map_x64, &map_w, &map_ws, nullptr, nullptr, &map_out};
   single_kernel_body<kFc1 ? kModeFc1 : kModeFc2, false>(m, m, a, a);
 }
 
@@ -894,12 +904,13 @@ template <bool kFc1>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_narrow_kernel(const __grid_constant__ CUtensorMap map_x128,
                            const __grid_constant__ CUtensorMap map_x16,
+                           const __grid_constant__ CUtensorMap map_x64,
                            const __grid_constant__ CUtensorMap map_w,
                            const __grid_constant__ CUtensorMap map_ws,
                            const __grid_constant__ CUtensorMap map_w64,
                            const __grid_constant__ CUtensorMap map_ws64,
                            const __grid_constant__ CUtensorMap map_out, GemmArgs a) {
-  const SingleMaps m{&map_x128, &map_x16, &map_w, &map_ws, &map_w64, &map_ws64, &map_out};
+  const SingleMaps m{&map_x128, &map_x16, &map_x64, &map_w, &map_ws, &map_w64, &map_ws64, &map_out};
   single_kernel_body<kFc1 ? kModeFc1 : kModeFc2, true>(m, m, a, a);
 }
 
@@ -909,6 +920,7 @@ template <bool kNarrow>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_fused_kernel(const __grid_constant__ CUtensorMap f1_x128,
                           const __grid_constant__ CUtensorMap f1_x16,
+                          const __grid_constant__ CUtensorMap f1_x64,
                           const __grid_constant__ CUtensorMap f1_w,
                           const __grid_constant__ CUtensorMap f1_ws,
                           const __grid_constant__ CUtensorMap f1_w64,
@@ -916,13 +928,14 @@ grouped_gemm_fused_kernel(const __grid_constant__ CUtensorMap f1_x128,
                           const __grid_constant__ CUtensorMap f1_out,
                           const __grid_constant__ CUtensorMap f2_x128,
                           const __grid_constant__ CUtensorMap f2_x16,
+                          const __grid_constant__ CUtensorMap f2_x64,
                           const __grid_constant__ CUtensorMap f2_w,
                           const __grid_constant__ CUtensorMap f2_ws,
                           const __grid_constant__ CUtensorMap f2_w64,
                           const __grid_constant__ CUtensorMap f2_ws64,
                           const __grid_constant__ CUtensorMap f2_out, GemmArgs a1, GemmArgs a2) {
-  const SingleMaps m1{&f1_x128, &f1_x16, &f1_w, &f1_ws, &f1_w64, &f1_ws64, &f1_out};
-  const SingleMaps m2{&f2_x128, &f2_x16, &f2_w, &f2_ws, &f2_w64, &f2_ws64, &f2_out};
+  const SingleMaps m1{&f1_x128, &f1_x16, &f1_x64, &f1_w, &f1_ws, &f1_w64, &f1_ws64, &f1_out};
+  const SingleMaps m2{&f2_x128, &f2_x16, &f2_x64, &f2_w, &f2_ws, &f2_w64, &f2_ws64, &f2_out};
   single_kernel_body<kModeFused, kNarrow>(m1, m2, a1, a2);
 }
 
@@ -1528,11 +1541,11 @@ moe_status launch_gemm(const moe_problem& p, const moe_ws_layout& L, const void*
     if (kFc1 && g.narrow) as.prefetch_kb = narrow_prefetch_kb(grid);
     if (g.narrow)
       err = launch_pdl(grouped_gemm_narrow_kernel<kFc1>, dim3(static_cast<unsigned>(grid)),
-                       dim3(kThreads), kSingleSmemBytes, s, g.mx128, g.mx16, g.mw128, g.mws128,
-                       g.mw64, g.mws64, g.mout, as);
+                       dim3(kThreads), kSingleSmemBytes, s, g.mx128, g.mx16, g.mx64, g.mw128,
+                       g.mws128, g.mw64, g.mws64, g.mout, as);
     else
       err = launch_pdl(grouped_gemm_kernel<kFc1>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
-                       kSingleSmemBytes, s, g.mx128, g.mx16, g.mw128, g.mws128, g.mout, as);
+                       kSingleSmemBytes, s, g.mx128, g.mx16, g.mx64, g.mw128, g.mws128, g.mout, as);
   }
   if (err == cudaSuccess && g.pair_bound > 0) {
     int64_t clusters = g.max_clusters;
@@ -1596,14 +1609,14 @@ moe_status launch_fc12(const moe_problem& p, const moe_ws_layout& L, const void*
   cudaError_t err;
   if (g1.narrow)
     err = launch_pdl(grouped_gemm_fused_kernel<true>, dim3(static_cast<unsigned>(grid)),
-                     dim3(kThreads), kSingleSmemBytes, s, g1.mx128, g1.mx16, g1.mw128, g1.mws128,
-                     g1.mw64, g1.mws64, g1.mout, g2.mx128, g2.mx16, g2.mw128, g2.mws128, g2.mw64,
-                     g2.mws64, g2.mout, a1, a2);
+                     dim3(kThreads), kSingleSmemBytes, s, g1.mx128, g1.mx16, g1.mx64, g1.mw128,
+                     g1.mws128, g1.mw64, g1.mws64, g1.mout, g2.mx128, g2.mx16, g2.mx64, g2.mw128,
+                     g2.mws128, g2.mw64, g2.mws64, g2.mout, a1, a2);
   else
     err = launch_pdl(grouped_gemm_fused_kernel<false>, dim3(static_cast<unsigned>(grid)),
-                     dim3(kThreads), kSingleSmemBytes, s, g1.mx128, g1.mx16, g1.mw128, g1.mws128,
-                     g1.mw64, g1.mws64, g1.mout, g2.mx128, g2.mx16, g2.mw128, g2.mws128, g2.mw64,
-                     g2.mws64, g2.mout, a1, a2);
+                     dim3(kThreads), kSingleSmemBytes, s, g1.mx128, g1.mx16, g1.mx64, g1.mw128,
+                     g1.mws128, g1.mw64, g1.mws64, g1.mout, g2.mx128, g2.mx16, g2.mx64, g2.mw128,
+                     g2.mws128, g2.mw64, g2.mws64, g2.mout, a1, a2);
   if (err != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "grouped_gemm launch: %s", cudaGetErrorString(err));
   return MOE_OK;
