@@ -247,6 +247,9 @@ SMALL_CASES = [
     (1000, 256, 256, 8, 1, 0, "one_expert"),   # one expert holds every row (7 full tiles + 104)
     (1100, 256, 256, 4, 1, 0, "one_expert"),   # CTA pairs: 4 units + 76 rows (weight-major)
     (1200, 384, 320, 4, 1, 0, "one_expert"),   # CTA pairs: 4 units + 176 rows (masked pair)
+    (1034, 256, 192, 4, 1, 0, "one_expert"),   # CTA pairs: 4 units + 10 rows (64-row X box, 8 used)
+    (150, 256, 192, 4, 1, 0, "one_expert"),    # single-SM: 1 full tile + 22 rows (16-row X boxes)
+    (180, 256, 192, 4, 1, 0, "one_expert"),    # single-SM: 1 full tile + 52 rows (64-row X box)
     (2200, 256, 192, 4, 2, 256, "route"),      # CTA pairs for routed and shared groups
     (513, 128, 128, 8, 8, 0, "route"),         # k = E: every expert every token
     (200, 192, 128, 16, 4, 128, "random_dup"), # repeated ids in a row, shared expert
