@@ -223,19 +223,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// 3-D tiled load delivered to the same smem offset of every CTA in `mask`, completing
-// on the barrier at the same offset in each of them.
-__device__ __forceinline__ void tma_load_3d_multicast(void* dst, const CUtensorMap* map,
-                                                      uint64_t* bar, int32_t c0, int32_t c1,
-                                                      int32_t c2, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
-      "h"(mask)
-      : "memory");
-}
-
 // Bulk prefetch of a 2-D / 3-D tile into L2 (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
