@@ -5,9 +5,12 @@ then moe_forward (permute, FC1+SwiGLU, FC2, finalize), inputs resident in HBM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-Prints one JSON line (rank 0). Under torchrun with N > 1 every rank runs its own
-replica of the workload (tokens are independent: no data-path collective) and the
-job value is the tokens of all ranks over the slowest rank's time.
+Prints one JSON line (rank 0). Its headline value is the workload named by --workload
+(mixtral_prefill by default); ``per_config`` adds the five target workloads (tiny,
+mixtral_prefill, qwen3_decode, dsv3_layer, skewed), each measured the same way (step time,
+layer and GEMM roofline fractions, end to end, clocks). Under torchrun with N > 1 every
+rank runs its own replica of the workload (tokens are independent: no data-path
+collective) and the job value is the tokens of all ranks over the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -15,6 +18,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -35,6 +39,12 @@ from workloads import WORKLOADS, Workload, make_inputs, flops, min_bytes  # noqa
 METRIC = "MoE layer tokens/sec at 1 GB300 and % of roofline (HBM or bf16 TC)"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "mixtral_prefill"
+# The five workloads the layer's targets are stated on, in this order.
+TARGET_WORKLOADS = ["tiny", "mixtral_prefill", "qwen3_decode", "dsv3_layer", "skewed"]
+L2_NOTE = ("GPU arm: flushed between steps outside the step events (256 MiB write, then a "
+           "256 MiB read that writes its dirty lines back); CPU oracle arm: no flush")
+LAUNCH_NOTE = ("GPU arm: moe_route + moe_forward captured once as a CUDA graph, replayed per "
+               "step; CPU oracle arm: routing + fp64 layer on a bounded token sample per step")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -178,6 +188,59 @@ def cpu_baseline(w: Workload, inp_host: dict, target_s: float = 10.0):
             "sample": f"{n} of {w.T} tokens of {w.name} (routing + fp64 layer), {dt:.1f} s"}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+_SINGLE_CORE_SCRIPT = r"""
+import json, sys, time
+import torch
+sys.path.insert(0, sys.argv[1])
+import oracle
+from workloads import WORKLOADS, make_inputs
+out = {}
+for name in sys.argv[2:]:
+    w = WORKLOADS[name]
+    inp = make_inputs(w, device="cpu", seed=0)
+    h = {n: None if v is None else v.float().numpy() for n, v in inp.items()}
+    torch.set_num_threads(1)   # the draw above may use every core; the timed oracle one
+    t0 = time.perf_counter()
+    ids, sc = oracle.route(h["logits"], w.method, w.k, bias=h["bias"], n_group=w.n_group,
+                           topk_group=w.topk_group, routed_scaling_factor=w.rsf)
+    oracle.forward(h["x"], ids, sc, h["w13"], h["w2"], h["w13_s"], h["w2_s"])
+    dt = time.perf_counter() - t0
+    out[name] = {"value": round(w.T / dt, 2), "unit": "tokens/s", "tokens": w.T,
+                 "seconds": round(dt, 3)}
+print(json.dumps(out))
+"""
+
+
+def single_core_oracle(names=("tiny", "qwen3_decode")):
+    """The oracle on one host core (BLAS and torch limited to one thread), whole batches of
+    the two small target workloads. Runs in a child process so the thread limits apply."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", _SINGLE_CORE_SCRIPT, ROOT, *names], env=env,
+                           capture_output=True, text=True, timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"error": f"single-core oracle run failed: {e!r}"[:200]}
+
+
 # --------------------------------------------------------------------------- ranks
 
 def reduce_max(value: float, world: int, device=None) -> float:
@@ -209,11 +272,40 @@ def traffic_record(kernel_file: str, workload: str):
     return rec.get("dram_bytes_per_launch")
 
 
-def run_ours(args, rank, world):
+def workload_config(w: Workload, world: int) -> dict:
+    """The `config` object of the JSON line; both arms print the same one."""
+    return {"workload": w.describe(), "T": w.T, "H": w.H, "I": w.I, "E": w.E, "k": w.k,
+            "routing_method": w.method, "n_group": w.n_group, "topk_group": w.topk_group,
+            "routed_scaling_factor": w.rsf, "shared_I": w.shared_I, "l2": L2_NOTE,
+            "launch": LAUNCH_NOTE,
+            "parallelism": f"replicas x{world} (no collective on the data path)"}
+
+
+def gemm_roofline(w: Workload, n_active: int, ms: float, peaks: dict):
+    """Roofline of the step's one GEMM launch (FC1 + SwiGLU + FC2). Algorithmic work per
+    launch: both GEMMs' flops; bytes = the active experts' w13 and w2 (+ the shared
+    expert's), the x_perm rows read, h written and read back, out_perm written."""
+    P_tc = peaks["bf16_tflops"]
+    rows_r, rows_s = w.P, (w.T if w.shared_I else 0)
+    g_flops = 2.0 * w.P * 3 * w.I * w.H + 2.0 * w.T * 3 * w.shared_I * w.H
+    g_bytes = (n_active * 3 * w.I * w.H + 3 * w.shared_I * w.H) * 2 + \
+        (rows_r + rows_s) * w.H * 2 * 2 + (rows_r * w.I + rows_s * w.shared_I) * 2 * 2
+    t = ms * 1e-3
+    if g_flops / (P_tc * 1e12) >= g_bytes / (peaks["hbm_gbs"] * 1e9):
+        ach = g_flops / t / 1e12
+        return {"bound": "tensor", "achieved": round(ach, 1), "peak": P_tc, "unit": "TFLOP/s",
+                "frac": round(ach / P_tc, 4)}, g_flops, g_bytes
+    ach = g_bytes / t / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(ach / peaks["hbm_gbs"], 4)}, g_flops, g_bytes
+
+
+def measure(name: str, args, rank: int, world: int, dev, headline: bool) -> dict:
+    """One workload: the timed step, the per-kernel times, the end-to-end run and the
+    rooflines. `headline` adds the gate kernel, the separate FC1 / FC2 launches and the
+    CPU baseline, and returns the full JSON line; otherwise a compact summary."""
     import mixture_experts_layer_03_gb300 as moe
-    w = WORKLOADS[args.workload]
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
+    w = WORKLOADS[name]
     inp = make_inputs(w, device=dev, seed=rank)
     if w.in_dtype == "f32":
         x = moe.moe_cast_f32_to_bf16(inp["x"])
@@ -238,7 +330,7 @@ def run_ours(args, rank, world):
         moe.moe_forward(xx, ids, sc, w13, w2, w13s, w2s, y=y, workspace=ws, stream=s)
 
     # route; permute (the histogram kernel only with more than one 1024-pair chunk, the
-    # plan kernel, the row gather); FC1 and FC2 in one persistent GEMM launch (CTA-pair
+    # plan kernel, the row copy); FC1 and FC2 in one persistent GEMM launch (CTA-pair
     # kernel when T*k >= 256*E, else single-SM); finalize
     launches_per_step = 1 + (3 if ws.layout["n_chunks"] > 1 else 2) + 1 + 1
     for _ in range(args.warmup):
@@ -286,7 +378,8 @@ def run_ours(args, rank, world):
     # ---- per-kernel durations: the same kernels through the step entry points, queued
     # behind a sleep kernel so each event pair brackets device time only.
     # fc1_fc2 is the step's GEMM launch (both GEMMs, one persistent kernel); fc1 and fc2
-    # are the same GEMMs launched one at a time (the step entry points), for reference.
+    # (headline workload only) are the same GEMMs launched one at a time (the step entry
+    # points), for reference.
     reps = max(3, min(args.steps, 10))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(reps)]
     torch.cuda.synchronize()
@@ -303,55 +396,60 @@ def run_ours(args, rank, world):
         e[3].record(stream)
         moe.moe_finalize(p, sc, y, ws, stream=stream)
         e[4].record(stream)
-        flush(i)
-        e[5].record(stream)
-        moe.moe_fc1(p, w13, w13s, ws, stream=stream)
-        e[6].record(stream)
-        moe.moe_fc2(p, w2, w2s, ws, stream=stream)
-        e[7].record(stream)
+        if headline:
+            flush(i)
+            e[5].record(stream)
+            moe.moe_fc1(p, w13, w13s, ws, stream=stream)
+            e[6].record(stream)
+            moe.moe_fc2(p, w2, w2s, ws, stream=stream)
+            e[7].record(stream)
     torch.cuda.synchronize()
-    pairs = {"route": (0, 1), "permute": (1, 2), "fc1_fc2": (2, 3), "finalize": (3, 4),
-             "fc1": (5, 6), "fc2": (6, 7)}
+    pairs = {"route": (0, 1), "permute": (1, 2), "fc1_fc2": (2, 3), "finalize": (3, 4)}
+    if headline:
+        pairs.update({"fc1": (5, 6), "fc2": (6, 7)})
     kern_ms = {n: statistics.median([evs[i][a].elapsed_time(evs[i][b]) for i in range(reps)])
                for n, (a, b) in pairs.items()}
 
-    peaks_early, _ = load_peaks()
-    # ---- the router gate (logits = x . wg^T; with a shared expert its gate is fused in as
-    # one more row), not part of the timed step (the step takes the logits as input):
-    # timed on this workload's x with a seeded N(0, H^-1/2) gate matrix.
-    n_sh = 1 if w.shared_I else 0
-    wg = (torch.randn(w.E + n_sh, w.H, generator=torch.Generator(device=dev).manual_seed(7),
-                      device=dev) * w.H ** -0.5).to(torch.bfloat16)
-    lg_g = torch.empty((w.T, w.E), dtype=torch.float32, device=dev)
-    sg_g = torch.empty((w.T,), dtype=torch.float32, device=dev) if n_sh else None
-    for _ in range(3):
-        moe.moe_gate(x, wg, w.E, lg_g, sg_g, stream=stream)
-    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(reps)]
-    torch.cuda.synchronize()
-    torch.cuda._sleep(20_000_000)
-    for i in range(reps):
-        flush(i)
-        gev[i][0].record(stream)
-        moe.moe_gate(x, wg, w.E, lg_g, sg_g, stream=stream)
-        gev[i][1].record(stream)
-    torch.cuda.synchronize()
-    gate_ms = statistics.median(a.elapsed_time(b) for a, b in gev)
-    g_flops = 2.0 * w.T * w.H * (w.E + n_sh)
-    g_bytes = 2.0 * (w.T + w.E + n_sh) * w.H + 4.0 * w.T * (w.E + n_sh)
-    g_tc = g_flops / (peaks_early["bf16_tflops"] * 1e12) >= g_bytes / (peaks_early["hbm_gbs"] * 1e9)
-    gate = {"ms": round(gate_ms, 4), "rows": w.E + n_sh, "bound": "tensor" if g_tc else "hbm",
-            "achieved": round((g_flops / 1e12 if g_tc else g_bytes / 1e9) / (gate_ms * 1e-3), 1),
-            "unit": "TFLOP/s" if g_tc else "GB/s"}
-    gate["frac"] = round(gate["achieved"] / (peaks_early["bf16_tflops"] if g_tc else
-                                            peaks_early["hbm_gbs"]), 4)
+    peaks, peak_src = load_peaks()
+    gate = None
+    if headline:
+        # ---- the router gate (logits = x . wg^T; with a shared expert its gate is fused
+        # in as one more row), not part of the timed step (the step takes the logits as
+        # input): timed on this workload's x with a seeded N(0, H^-1/2) gate matrix.
+        n_sh = 1 if w.shared_I else 0
+        wg = (torch.randn(w.E + n_sh, w.H, generator=torch.Generator(device=dev).manual_seed(7),
+                          device=dev) * w.H ** -0.5).to(torch.bfloat16)
+        lg_g = torch.empty((w.T, w.E), dtype=torch.float32, device=dev)
+        sg_g = torch.empty((w.T,), dtype=torch.float32, device=dev) if n_sh else None
+        for _ in range(3):
+            moe.moe_gate(x, wg, w.E, lg_g, sg_g, stream=stream)
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(20_000_000)
+        for i in range(reps):
+            flush(i)
+            gev[i][0].record(stream)
+            moe.moe_gate(x, wg, w.E, lg_g, sg_g, stream=stream)
+            gev[i][1].record(stream)
+        torch.cuda.synchronize()
+        gate_ms = statistics.median(a.elapsed_time(b) for a, b in gev)
+        g_flops = 2.0 * w.T * w.H * (w.E + n_sh)
+        g_bytes = 2.0 * (w.T + w.E + n_sh) * w.H + 4.0 * w.T * (w.E + n_sh)
+        g_tc = g_flops / (peaks["bf16_tflops"] * 1e12) >= g_bytes / (peaks["hbm_gbs"] * 1e9)
+        gate = {"ms": round(gate_ms, 4), "rows": w.E + n_sh, "bound": "tensor" if g_tc else "hbm",
+                "achieved": round((g_flops / 1e12 if g_tc else g_bytes / 1e9) / (gate_ms * 1e-3), 1),
+                "unit": "TFLOP/s" if g_tc else "GB/s"}
+        gate["frac"] = round(gate["achieved"] / (peaks["bf16_tflops"] if g_tc else
+                                                peaks["hbm_gbs"]), 4)
 
     # ---- end to end through the public API: every step copies its inputs (x, logits)
     # in from pinned host memory and its result (y) out to pinned host memory. Three
     # streams and two device buffer sets let step i's copy-out and step i+1's copy-in run
     # beside step i's compute; a buffer set is reused only after the copy-out of the
     # step that last used it. The timed region runs from the first copy-in to the last
-    # copy-out. No L2 flush here: each step's inputs (the expert weights) exceed L2.
+    # copy-out. No L2 flush here: each step's inputs (the expert weights) exceed L2,
+    # except for the tiny workload, whose steps are bound by launch latency.
     x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     x_h.copy_(x)
     lg_h = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
@@ -403,38 +501,21 @@ def run_ours(args, rank, world):
     assert torch.equal(y_h[(n - 1) & 1], y_d[(n - 1) & 1].cpu()), "copied-out result differs"
     st, flags = moe.moe_read_device_status(ws)
     if st != moe.MOE_OK:
-        raise RuntimeError(f"device status {st} flags {flags}")
+        raise RuntimeError(f"{name}: device status {st} flags {flags}")
 
     # ---- roofline of the dominant kernel and of the whole layer
-    peaks, peak_src = load_peaks()
-    P_tc = peaks["bf16_tflops"]
-    # The dominant kernel: the step's one GEMM launch (FC1 + SwiGLU + FC2). Algorithmic
-    # work per launch: both GEMMs' flops; bytes = the active experts' w13 and w2 (+ the
-    # shared expert's), the x_perm rows read, h written and read back, out_perm written.
-    rows_r, rows_s = w.P, (w.T if w.shared_I else 0)
-    g_flops = 2.0 * w.P * 3 * w.I * w.H + 2.0 * w.T * 3 * w.shared_I * w.H
-    g_bytes = (n_active * 3 * w.I * w.H + 3 * w.shared_I * w.H) * 2 + \
-        (rows_r + rows_s) * w.H * 2 * 2 + (rows_r * w.I + rows_s * w.shared_I) * 2 * 2
-    g_t = kern_ms["fc1_fc2"] * 1e-3
-    tensor_bound = g_flops / (P_tc * 1e12) >= g_bytes / (peaks["hbm_gbs"] * 1e9)
-    if tensor_bound:
-        ach = g_flops / g_t / 1e12
-        roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": P_tc, "unit": "TFLOP/s",
-                    "frac": round(ach / P_tc, 4)}
-    else:
-        ach = g_bytes / g_t / 1e9
-        roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4)}
-    roofline.update({"traffic": traffic_record("grouped_gemm.cu", args.workload),
+    roofline, g_flops, g_bytes = gemm_roofline(w, n_active, kern_ms["fc1_fc2"], peaks)
+    roofline.update({"traffic": traffic_record("grouped_gemm.cu", name),
                      "kernel": "grouped GEMM FC1+SwiGLU+FC2, one persistent launch "
                                "(CTA-pair or single-SM kernel)",
-                     "peak_source": f"{peak_src} ({'bf16_tflops burst' if tensor_bound else 'hbm_gbs'})",
+                     "peak_source": f"{peak_src} ("
+                                    f"{'bf16_tflops burst' if roofline['bound'] == 'tensor' else 'hbm_gbs'})",
                      "algorithmic_flops_per_launch": g_flops,
                      "algorithmic_bytes_per_launch": g_bytes,
                      "ms_per_launch": round(kern_ms["fc1_fc2"], 4)})
     fl = flops(w)
     by = min_bytes(w, n_active)
-    t_tc, t_hbm = fl / (P_tc * 1e12), by / (peaks["hbm_gbs"] * 1e9)
+    t_tc, t_hbm = fl / (peaks["bf16_tflops"] * 1e12), by / (peaks["hbm_gbs"] * 1e9)
     t_roof = max(t_tc, t_hbm)
     layer = {"bound": "tensor" if t_tc >= t_hbm else "hbm",
              "t_roof_ms": round(t_roof * 1e3, 4), "t_ms": round(ms_per_step, 4),
@@ -442,26 +523,58 @@ def run_ours(args, rank, world):
              "n_active_experts": n_active,
              "achieved_tflops": round(fl / (ms_per_step * 1e-3) / 1e12, 1),
              "achieved_gbs": round(by / (ms_per_step * 1e-3) / 1e9, 1),
-             "peaks": f"{peak_src}: hbm_gbs {peaks['hbm_gbs']}, bf16_tflops (burst) {P_tc}"}
+             "peaks": f"{peak_src}: hbm_gbs {peaks['hbm_gbs']}, bf16_tflops (burst) "
+                      f"{peaks['bf16_tflops']}"}
 
+    if not headline:
+        return {"ms_per_step": round(ms_per_step, 4), "tokens_per_s": round(value, 1),
+                "layer": {k: layer[k] for k in ("bound", "frac", "t_roof_ms", "n_active_experts")},
+                "gemm": {k: roofline[k] for k in ("bound", "achieved", "unit", "frac", "traffic",
+                                                  "ms_per_launch")},
+                "kernels_ms": {n_: round(v, 4) for n_, v in kern_ms.items()},
+                "e2e_tokens_per_s": e2e["value"], "gpu_launches": launches_per_step * args.steps,
+                "clocks": clocks}
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations/logits, N(0, fan_in^-1/2) random-init weights)",
-        "config": {"workload": w.describe(), "T": w.T, "H": w.H, "I": w.I, "E": w.E, "k": w.k,
-                   "routing_method": w.method, "shared_I": w.shared_I,
-                   "l2": (f"flushed between steps outside the step events: {L2_FLUSH_BYTES >> 20} MiB "
-                          f"write, then a {L2_FLUSH_BYTES >> 20} MiB read that writes its dirty lines back"),
-                   "launch": "moe_route + moe_forward captured once as a CUDA graph, replayed per step",
-                   "parallelism": f"replicas x{world} (no collective on the data path)"},
+        "config": workload_config(w, world),
         "roofline": roofline, "layer_roofline": layer,
-        "kernels_ms": {n: round(v, 4) for n, v in kern_ms.items()},
+        "kernels_ms": {n_: round(v, 4) for n_, v in kern_ms.items()},
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
         "gate_kernel": gate,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, host_inputs(inp))
+        cb = cpu_baseline(w, host_inputs(inp))
+        cb["cpu_model"] = cpu_model()
+        cb["single_core"] = single_core_oracle()
+        result["cpu_baseline"] = cb
+    return result
+
+
+def run_ours(args, rank, world):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    result = measure(args.workload, args, rank, world, dev, headline=True)
+    torch.cuda.empty_cache()
+    if args.per_config:
+        per = {}
+        for name in TARGET_WORKLOADS:
+            if name == args.workload:
+                per[name] = {"ms_per_step": result["ms_per_step"], "tokens_per_s": result["value"],
+                             "layer": {k: result["layer_roofline"][k] for k in
+                                       ("bound", "frac", "t_roof_ms", "n_active_experts")},
+                             "gemm": {k: result["roofline"][k] for k in
+                                      ("bound", "achieved", "unit", "frac", "traffic",
+                                       "ms_per_launch")},
+                             "kernels_ms": result["kernels_ms"],
+                             "e2e_tokens_per_s": result["e2e"]["value"],
+                             "gpu_launches": result["gpu_launches"], "clocks": result["clocks"]}
+                continue
+            per[name] = measure(name, args, rank, world, dev, headline=False)
+            torch.cuda.empty_cache()
+        result["per_config"] = per
     return result
 
 
@@ -482,12 +595,14 @@ def run_reference(args):
         total_n += n
     value = total_n / total_t
     cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    world = int(os.environ.get("WORLD_SIZE", 1))
     return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total_t / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.describe(), "T": w.T, "H": w.H, "I": w.I, "E": w.E, "k": w.k},
+            "config": workload_config(w, world),
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "cpu_model": cpu_model(),
                              "sample": f"{per_step} of {w.T} tokens per step (routing + fp64 layer)"},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
@@ -502,6 +617,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="measure the headline workload only (no per_config object)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -18,7 +18,8 @@
  *    library allocates no device memory; the forward uses the caller's
  *    workspace (size from moe_workspace_bytes).
  *  - `stream` is a cudaStream_t (passed as void*). Work is enqueued on it
- *    only; no call below synchronises except moe_read_device_status.
+ *    only; no call below synchronises except moe_read_device_status and
+ *    moe_static_read_device_status.
  *  - bf16 tensors are passed as void* to 2-byte IEEE bfloat16 elements,
  *    row-major, innermost dimension contiguous. Every device pointer must be
  *    16-byte aligned.
@@ -201,14 +202,23 @@ moe_status moe_forward(const moe_problem* p, const void* x, const int32_t* ids, 
  *  - Every call on a device shares the one array and it keeps the previous call's
  *    contents (the call clears what must start at zero itself). Calls whose work
  *    overlaps on the GPU race: order them on one stream.
- *  - Device-detected errors (ids outside [0, E)) skip rows as in moe_forward; their
- *    status bits stay in the library's array and are not reported.
+ *  - Device-detected errors (ids outside [0, E), a bounded wait that ran out) skip rows
+ *    as in moe_forward and set the status word inside the array, which each call clears
+ *    when it starts; moe_static_read_device_status reads it back.
  * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  */
 #define MOE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 moe_status moe_forward_static(const moe_problem* p, const void* x, const int32_t* ids,
                               const float* scales, const void* w13, const void* w2,
                               const void* w13_s, const void* w2_s, void* y, void* stream);
+
+/* The status word of moe_forward_static on the current device: synchronises `stream`
+ * (the stream the forward ran on), reads and clears the word inside the library's
+ * scratch array. *flags (may be NULL) receives the MOE_DEVICE_FLAG_* bits. Returns
+ * MOE_ERR_DEVICE_BAD_ID or MOE_ERR_DEVICE_TIMEOUT when a bit is set, else MOE_OK;
+ * MOE_ERR_CUDA if the copy or the device lookup fails. Like the forward, it allocates
+ * nothing; the word is shared by every caller of moe_forward_static on the device. */
+moe_status moe_static_read_device_status(void* stream, int32_t* flags);
 
 /* Router gate (vLLM MoE page, section "Gate 计算与 FSE"): router logits = x . wg^T with
  * fp32 accumulation, one GEMM for the routed experts' gate and, with n_shared = 1, the

@@ -81,6 +81,7 @@ _SIGS = {
                                    _P]),
     "moe_finalize": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_read_device_status": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
+    "moe_static_read_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32)]),
     "moe_selftest_wait": (ctypes.c_int, [_P, _P]),
     "moe_cast_f32_to_bf16": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P]),
 }
@@ -335,6 +336,14 @@ def moe_read_device_status(workspace: Workspace, stream=None):
     """Synchronise, read and clear the device status word. Returns (status, flags)."""
     flags = ctypes.c_int32(0)
     st = _lib.moe_read_device_status(workspace.ptr, _stream(stream), ctypes.byref(flags))
+    return st, flags.value
+
+
+def moe_static_read_device_status(stream=None):
+    """Synchronise, read and clear moe_forward_static's status word on the current device.
+    Returns (status, flags)."""
+    flags = ctypes.c_int32(0)
+    st = _lib.moe_static_read_device_status(_stream(stream), ctypes.byref(flags))
     return st, flags.value
 
 

@@ -333,6 +333,20 @@ moe_status static_scratch_base(char** base) {
   return MOE_OK;
 }
 
+// Reads the status word at `status` after the work queued on `s`, then clears it.
+moe_status read_status_word(void* status, cudaStream_t s, int32_t* flags) {
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, status, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(v), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (flags) *flags = v;
+  if (v & MOE_DEVICE_FLAG_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
+  if (v & MOE_DEVICE_FLAG_BAD_ID) return MOE_ERR_DEVICE_BAD_ID;
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -370,17 +384,14 @@ moe_status moe_forward_static(const moe_problem* p, const void* x, const int32_t
 
 moe_status moe_read_device_status(void* workspace, void* stream, int32_t* flags) {
   if (!workspace) return set_error(MOE_ERR_INVALID_ARG, "workspace is NULL");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int32_t v = 0;
-  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(v), s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
-  if (flags) *flags = v;
-  if (v & MOE_DEVICE_FLAG_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
-  if (v & MOE_DEVICE_FLAG_BAD_ID) return MOE_ERR_DEVICE_BAD_ID;
-  return MOE_OK;
+  return read_status_word(workspace, static_cast<cudaStream_t>(stream), flags);
+}
+
+moe_status moe_static_read_device_status(void* stream, int32_t* flags) {
+  char* ws = nullptr;
+  const moe_status st = static_scratch_base(&ws);
+  if (st != MOE_OK) return st;
+  return read_status_word(ws, static_cast<cudaStream_t>(stream), flags);
 }
 
 moe_status moe_selftest_wait(void* workspace, void* stream) {

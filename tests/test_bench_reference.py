@@ -29,8 +29,18 @@ def test_reference_arm_prints_one_contract_line():
     assert d["config"]["workload"].startswith("tiny:")
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert cb["cpu_model"]
+    # the same config object as the GPU arm prints for this workload
+    from workloads import WORKLOADS
+    assert d["config"] == bench.workload_config(WORKLOADS["tiny"], 1)
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_single_core_oracle_rate():
+    import bench
+    d = bench.single_core_oracle(("tiny",))
+    assert d["tiny"]["value"] > 0 and d["tiny"]["tokens"] == 64, d
 
 
 def test_reference_arm_other_ranks_exit_without_output():

@@ -391,7 +391,8 @@ def test_forward_with_the_fused_shared_gate(moe):
 
 @pytest.mark.parametrize("T,E,k", [(65536, 8, 8), (40000, 256, 8)])
 def test_largest_row_counts(moe, T, E, k):
-    """Many permuted rows (T*k up to 524,288): routing, the permutation and sampled y."""
+    """Many permuted rows (T*k up to 524,288): routing, the permutation and y on every
+    token."""
     H, I = 128, 64
     g = torch.Generator(device="cuda").manual_seed(T)
     logits = torch.randn(T, E, generator=g, device="cuda")
@@ -407,10 +408,9 @@ def test_largest_row_counts(moe, T, E, k):
     assert np.array_equal(ids.cpu().numpy(), ids_ref)
     counts, offsets, perm_src, perm_inv = oracle.permute(ids_ref, E)
     assert np.array_equal(ws.region("perm_src", T * k, torch.int32).cpu().numpy(), perm_src)
-    sample = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(1).choice(T, 24, replace=False)]))
-    y_ref = oracle.forward(x[sample].cpu().double().numpy(), ids_ref[sample], sc_ref[sample],
-                           ExpertView(w13), ExpertView(w2))
-    _check_close(y[sample].cpu().double().numpy(), y_ref, Y_TOL, "y (sampled)")
+    y_ref = oracle.forward(x.cpu().double().numpy(), ids_ref, sc_ref, ExpertView(w13),
+                           ExpertView(w2))
+    _check_close(y.cpu().double().numpy(), y_ref, Y_TOL, "y (every token)")
     st, flags = moe.moe_read_device_status(ws)
     assert st == moe.MOE_OK and flags == 0
 
@@ -556,8 +556,16 @@ def test_cast_is_round_to_nearest_even(moe):
 
 # ------------------------------------------------------------------------ full-size workloads
 
-SAMPLE_TOKENS = {"tiny": 64, "mixtral_prefill": 16, "qwen3_decode": 16, "dsv3_layer": 4,
-                 "skewed": 16, "llama4_scout": 6, "minimax_m2": 6}
+def _leftover_rows(offsets, unit):
+    """Permuted rows past each expert's last full unit of `unit` rows (the rows the GEMMs
+    cover with their partial, weight-major or masked units)."""
+    rows = []
+    for e in range(len(offsets) - 1):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        rem = (b - a) % unit
+        if rem:
+            rows.append(np.arange(b - rem, b))
+    return np.concatenate(rows) if rows else np.zeros(0, np.int64)
 
 
 @pytest.mark.slow
@@ -565,8 +573,11 @@ SAMPLE_TOKENS = {"tiny": 64, "mixtral_prefill": 16, "qwen3_decode": 16, "dsv3_la
                                   "llama4_scout", "minimax_m2"])
 def test_workload_full_size(moe, name):
     """The workloads at full size, in the launch configuration the bench times
-    (moe_route then moe_forward on one stream). Routing, counts and permutation are
-    checked on every token; y on sampled tokens (plus the edge tokens)."""
+    (moe_route then moe_forward on one stream). Routing, counts and the permutation are
+    checked on every token; y on every token, and the intermediate h (FC1 + SwiGLU) and
+    out_perm (FC2) rows on every permuted row, against the oracle's five-step forward.
+    The rows of each expert past its last full 256-row unit are named separately (the
+    GEMMs' partial units)."""
     w: Workload = WORKLOADS[name]
     inp = make_inputs(w, device="cuda", seed=0)
     if w.in_dtype == "f32":
@@ -595,20 +606,42 @@ def test_workload_full_size(moe, name):
     assert np.array_equal(ws.region("counts", w.E, torch.int32).cpu().numpy(), counts)
     assert np.array_equal(ws.region("perm_src", w.P, torch.int32).cpu().numpy(), perm_src)
     assert np.array_equal(ws.region("perm_inv", w.P, torch.int32).cpu().numpy(), perm_inv)
-
-    rng = np.random.default_rng(0)
-    n = min(SAMPLE_TOKENS[name], w.T)
-    sample = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, n, replace=False)]))
-    if w.in_dtype == "f32":   # the oracle takes the fp32 originals (the cast counts as error)
-        xs = inp["x"][sample].cpu().double().numpy()
-        W13, W2 = ExpertView(inp["w13"]), ExpertView(inp["w2"])
-    else:
-        xs = x[sample].cpu().double().numpy()
-        W13, W2 = ExpertView(w13), ExpertView(w2)
-    W13s = None if w13s is None else _np64(w13s)
-    W2s = None if w2s is None else _np64(w2s)
-    y_ref = oracle.forward(xs, ids_ref[sample], sc_ref[sample], W13, W2, W13s, W2s)
-    _check_close(y[sample].cpu().double().numpy(), y_ref, Y_TOL, f"{name} y (sampled)")
-    assert torch.isfinite(y.float()).all()
     st, flags = moe.moe_read_device_status(ws)
     assert st == moe.MOE_OK and flags == 0
+    assert torch.isfinite(y.float()).all()
+
+    if w.in_dtype == "f32":   # the oracle takes the fp32 originals (the cast counts as error)
+        X = inp["x"].cpu().double().numpy()
+        W13, W2 = ExpertView(inp["w13"]), ExpertView(inp["w2"])
+        W13s = W2s = None
+    else:
+        X = x.cpu().double().numpy()
+        W13, W2 = ExpertView(w13), ExpertView(w2)
+        W13s = None if w13s is None else _np64(w13s)
+        W2s = None if w2s is None else _np64(w2s)
+    # the oracle's weights are the oracle's own (fp64) scales, so the y comparison also
+    # carries the fp32 rounding of the device's scales
+    y_ref, inter = oracle.forward_permuted(X, ids_ref, sc_ref, W13, W2, W13s, W2s)
+    _check_close(y.cpu().double().numpy(), y_ref, Y_TOL, f"{name} y (every token)")
+
+    L = ws.layout
+    R, Ih = L["rows"], L["h_ld"]
+    P = w.P
+    h_ref, out_ref = inter["h"], inter["out"]
+    h_gpu = ws.region("h", R * Ih, torch.bfloat16).view(R, Ih)[:P, :w.I].cpu().double().numpy()
+    _check_close(h_gpu, h_ref, H_TOL, f"{name} h (every permuted row)")
+    out_gpu = ws.region("out_perm", R * w.H, torch.bfloat16).view(R, w.H).cpu().double().numpy()
+    _check_close(out_gpu[:P], out_ref, Y_TOL, f"{name} out_perm (every permuted row)")
+    left = _leftover_rows(offsets, 256)
+    if left.size:
+        hb = H_TOL * np.abs(h_ref).max()
+        ob = Y_TOL * np.abs(out_ref).max()
+        eh = np.abs(h_gpu[left] - h_ref[left]).max()
+        eo = np.abs(out_gpu[left] - out_ref[left]).max()
+        assert eh <= hb, f"{name} h on the {left.size} leftover rows: {eh:.4e} > {hb:.4e}"
+        assert eo <= ob, f"{name} out_perm on the {left.size} leftover rows: {eo:.4e} > {ob:.4e}"
+    if w.shared_I:
+        hs_ref = oracle.swiglu(X @ W13s.T, w.shared_I)
+        hs_gpu = ws.region("h", R * Ih, torch.bfloat16).view(R, Ih)[P:, :w.shared_I]
+        _check_close(hs_gpu.cpu().double().numpy(), hs_ref, H_TOL, f"{name} shared h")
+        _check_close(out_gpu[P:], hs_ref @ W2s.T, Y_TOL, f"{name} shared out_perm rows")
