@@ -30,6 +30,13 @@ with E_i a SwiGLU FFN. Readings taken where the pages are silent:
   the sigmoid in float64 rounded once to fp32, then an IEEE fp32 add of the
   bias. Group score = fl32(top1 + top2 of kappa within the group). Ties: lowest
   group index, then lowest expert index.
+* vLLM GroupedTopKRouter (VLLM, section "GroupedTopKRouter：分组的专家选择"), sigmoid
+  scoring: score s_e = sigmoid(l_e) in float64; selection key fl32(s_e), the score rounded
+  once to fp32; group score = the sum of the group's keys added in fp32 in expert order;
+  keep the topk_group best groups, then the k / topk_group best experts inside each of
+  them; weights = s_sel / sum(s_sel) * routed_scaling_factor. With softmax scoring the
+  group score is the sum of a softmax taken inside the group, 1 for every group, so the
+  group choice would rest on tie-breaking alone; that form is refused.
 * Output slots are listed by descending selection key.
 * SwiGLU: the first I rows of w13[e] are the gate projection (w1), the next I
   rows the up projection (w3): h = silu(gate) * up, silu(z) = z / (1 + e^-z).
@@ -49,7 +56,13 @@ RENORMALIZE_NAIVE = 4
 MINIMAX2 = 5
 SIGMOID_RENORM = 6
 
-METHODS = (DEFAULT, RENORMALIZE, DEEPSEEKV3, LLAMA4, RENORMALIZE_NAIVE, MINIMAX2, SIGMOID_RENORM)
+# vLLM's GroupedTopKRouter, by its scoring function. The codes lie outside the range of
+# TensorRT-LLM's RoutingMethodType (0-8).
+GROUPED_TOPK = 16
+GROUPED_TOPK_SOFTMAX = 17
+
+METHODS = (DEFAULT, RENORMALIZE, DEEPSEEKV3, LLAMA4, RENORMALIZE_NAIVE, MINIMAX2, SIGMOID_RENORM,
+           GROUPED_TOPK)
 
 
 # --------------------------------------------------------------------------- routing
@@ -106,6 +119,60 @@ def group_select(kappa: np.ndarray, n_group: int, topk_group: int):
     return groups, gscore
 
 
+def group_totals_fp32(keys: np.ndarray, n_group: int) -> np.ndarray:
+    """Per-group sums of fp32 keys [T, E] -> [T, n_group], added in fp32 in expert order
+    (((k0 + k1) + k2) + ...), each addition rounded to fp32."""
+    T, E = keys.shape
+    g = np.asarray(keys, np.float32).reshape(T, n_group, E // n_group)
+    acc = g[..., 0].copy()
+    for j in range(1, g.shape[-1]):
+        acc = (acc + g[..., j]).astype(np.float32)
+    return acc
+
+
+def grouped_topk(logits32: np.ndarray, top_k: int, n_group: int, topk_group: int,
+                 routed_scaling_factor: float = 1.0, scoring: str = "sigmoid"):
+    """vLLM GroupedTopKRouter._select_experts, in the order VLLM lists its steps:
+
+    1. view the logits as [T, n_group, experts_per_group];
+    2. score inside each group (sigmoid here: s = sigmoid(l) in float64, key = fl32(s));
+    3. group score = sum of the group's scores (fp32 keys added in expert order), keep the
+       topk_group best groups (ties: lower group index);
+    4. inside each kept group, the top_k / topk_group best experts (ties: lower index);
+    5. renormalise the chosen scores to sum 1, times routed_scaling_factor.
+    Slots are listed by descending key (ties: lower expert index).
+    """
+    if scoring == "softmax":
+        raise ValueError("grouped top-k with softmax scoring: a softmax taken inside each group "
+                         "sums to 1 in every group, so the group choice would rest on "
+                         "tie-breaking alone")
+    if scoring != "sigmoid":
+        raise ValueError(f"unknown scoring function {scoring!r}")
+    l32 = np.asarray(logits32, dtype=np.float32)
+    T, E = l32.shape
+    if n_group < 1 or E % n_group or not 1 <= topk_group <= n_group or top_k % topk_group:
+        raise ValueError("grouped top-k needs E % n_group == 0, 1 <= topk_group <= n_group and "
+                         "top_k % topk_group == 0")
+    epg = E // n_group
+    per = top_k // topk_group
+    if per > epg:
+        raise ValueError("top_k / topk_group exceeds the experts per group")
+    s64 = sigmoid64(_selection_logits(l32).astype(np.float64))
+    key = s64.astype(np.float32)
+    groups = topk_desc(group_totals_fp32(key, n_group), topk_group)      # [T, topk_group]
+    chosen = np.zeros((T, E), dtype=bool)
+    rows = np.arange(T)[:, None]
+    for r in range(topk_group):
+        g = groups[:, r]
+        cols = g[:, None] * epg + np.arange(epg)[None, :]
+        inner = topk_desc(key[rows, cols], per)                            # [T, per]
+        chosen[rows, np.take_along_axis(cols, inner, axis=1)] = True
+    ids = topk_desc(np.where(chosen, key, np.float32(-np.inf)), top_k)
+    ssel = np.take_along_axis(s64, ids, axis=1)
+    w = ssel / np.sum(ssel, axis=1, keepdims=True) * routed_scaling_factor
+    return ids.astype(np.int32), w
+
+
 def route(logits, method: int, top_k: int, bias=None, n_group: int = 1, topk_group: int = 1,
           routed_scaling_factor: float = 1.0):
     """Routing: logits [T, E] fp32 -> (ids int32 [T, k], scales float64 [T, k]).
@@ -119,6 +186,8 @@ def route(logits, method: int, top_k: int, bias=None, n_group: int = 1, topk_gro
       MiniMax2 (5)          sigmoid -> bias add -> top-k -> divide by the unbiased sum
       SigmoidRenorm (6)     sigmoid -> top-k -> divide by the selected sum
     VLLM, section "FusedTopKRouter": the same softmax/sigmoid -> top-k -> renormalize.
+    VLLM, section "GroupedTopKRouter": GROUPED_TOPK (16) = ``grouped_topk`` with sigmoid
+    scoring; GROUPED_TOPK_SOFTMAX (17) is refused (see ``grouped_topk``).
     """
     l32 = np.asarray(logits, dtype=np.float32)
     T, E = l32.shape
@@ -151,6 +220,9 @@ def route(logits, method: int, top_k: int, bias=None, n_group: int = 1, topk_gro
             s = sigmoid64(lsel)
             w = s / np.sum(s, axis=1, keepdims=True)
         return ids.astype(np.int32), w
+    if method in (GROUPED_TOPK, GROUPED_TOPK_SOFTMAX):
+        return grouped_topk(l32, top_k, n_group, topk_group, routed_scaling_factor,
+                            "sigmoid" if method == GROUPED_TOPK else "softmax")
     if method == DEEPSEEKV3:
         b = np.zeros(E, np.float32) if bias is None else np.asarray(bias, np.float32)
         s64, kappa = deepseek_keys(l32, b)

@@ -129,3 +129,39 @@ def test_shared_gate_without_sigmoid_is_caught(monkeypatch):
         return np.asarray(shared_gate, dtype=np.float64)[:, None]
     monkeypatch.setattr(om, "_shared_weight", bad_weight)
     _fails(pins.test_shared_gate_weight_limits_and_linearity)
+
+
+def test_vllm_top2_group_score_is_caught(monkeypatch, golden_dir):
+    def top2_totals(keys, n_group):
+        T, E = keys.shape
+        g = -np.sort(-keys.reshape(T, n_group, E // n_group), axis=-1)
+        return (g[..., 0] + g[..., 1]).astype(np.float32)
+    monkeypatch.setattr(om, "group_totals_fp32", top2_totals)
+    _fails(pins.test_golden_vllm_grouped, golden_dir)
+
+
+def test_vllm_global_topk_in_kept_groups_is_caught(monkeypatch, golden_dir):
+    def global_topk(l32, top_k, n_group, topk_group, rsf=1.0, scoring="sigmoid"):
+        T, E = l32.shape
+        s64 = om.sigmoid64(l32.astype(np.float64))
+        key = s64.astype(np.float32)
+        groups = om.topk_desc(om.group_totals_fp32(key, n_group), topk_group)
+        mask = np.zeros((T, n_group), bool)
+        np.put_along_axis(mask, groups, True, axis=1)
+        masked = np.where(np.repeat(mask, E // n_group, axis=1), key, np.float32(-np.inf))
+        ids = om.topk_desc(masked, top_k)
+        ssel = np.take_along_axis(s64, ids, axis=1)
+        return ids.astype(np.int32), ssel / ssel.sum(1, keepdims=True) * rsf
+    monkeypatch.setattr(om, "grouped_topk", global_topk)
+    _fails(pins.test_golden_vllm_grouped, golden_dir)
+
+
+def test_vllm_missing_renormalisation_is_caught(monkeypatch, golden_dir):
+    real = om.grouped_topk
+
+    def no_renorm(l32, top_k, n_group, topk_group, rsf=1.0, scoring="sigmoid"):
+        ids, _ = real(l32, top_k, n_group, topk_group, rsf, scoring)
+        s64 = om.sigmoid64(np.asarray(l32, np.float64))
+        return ids, np.take_along_axis(s64, ids.astype(np.int64), axis=1) * rsf
+    monkeypatch.setattr(om, "grouped_topk", no_renorm)
+    _fails(pins.test_golden_vllm_grouped, golden_dir)

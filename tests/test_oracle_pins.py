@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 from oracle import (DEFAULT, RENORMALIZE, DEEPSEEKV3, LLAMA4, RENORMALIZE_NAIVE, MINIMAX2,
-                    SIGMOID_RENORM)
+                    SIGMOID_RENORM, GROUPED_TOPK, GROUPED_TOPK_SOFTMAX)
 
 
 def _ev(expr):
@@ -50,6 +50,22 @@ def test_golden_grouped_deepseek(golden_dir):
                            topk_group=g["topk_group"],
                            routed_scaling_factor=g["routed_scaling_factor"])
     assert ids[0].tolist() == g["expected_ids"]
+    np.testing.assert_allclose(sc[0], [_ev(e) for e in g["expected_scales_expr"]], rtol=1e-6)
+
+
+def test_golden_vllm_grouped(golden_dir):
+    g = _load(golden_dir, "route_vllm_grouped_hand.json")
+    p = np.array(g["probabilities"], np.float64)
+    logits = np.log(p / (1 - p)).astype(np.float32)[None, :]
+    key = oracle.sigmoid64(logits.astype(np.float64)).astype(np.float32)
+    epg = g["E"] // g["n_group"]
+    sums = [sum(g["probabilities"][j * epg:(j + 1) * epg]) for j in range(g["n_group"])]
+    np.testing.assert_allclose(oracle.group_totals_fp32(key, g["n_group"])[0], sums, rtol=1e-6)
+    ids, sc = oracle.route(logits, GROUPED_TOPK, g["top_k"], n_group=g["n_group"],
+                           topk_group=g["topk_group"],
+                           routed_scaling_factor=g["routed_scaling_factor"])
+    assert ids[0].tolist() == g["expected_ids"]
+    assert sorted({e // epg for e in ids[0].tolist()}) == sorted(g["expected_groups"])
     np.testing.assert_allclose(sc[0], [_ev(e) for e in g["expected_scales_expr"]], rtol=1e-6)
 
 
@@ -236,6 +252,85 @@ def test_grouped_single_group_reduces_to_sigmoid_renorm():
     same = (ia == ib).all(1)
     assert same.mean() > 0.9
     np.testing.assert_allclose(sa[same], sb[same], rtol=1e-12)
+
+
+def _vllm_grouped_brute(logit, n_group, topk_group, k, rsf):
+    """vLLM grouped top-k by enumeration: the group totals added one fp32 step at a time in
+    expert order; the topk_group-subset of groups with the largest sum of totals (then the
+    lexicographically smallest index tuple, i.e. lower group indices win ties); inside each
+    kept group its k / topk_group experts by rank counting; slots by rank counting over the
+    union; weights from explicit loops over the float64 sigmoid."""
+    E = len(logit)
+    epg = E // n_group
+    per = k // topk_group
+    s = [1 / (1 + math.exp(-float(v))) for v in logit]
+    key = [float(np.float32(si)) for si in s]
+    totals = []
+    for g in range(n_group):
+        acc = np.float32(key[g * epg])
+        for j in range(1, epg):
+            acc = np.float32(acc + np.float32(key[g * epg + j]))
+        totals.append(float(acc))
+    best = None
+    for sub in itertools.combinations(range(n_group), topk_group):
+        tot = sum(totals[g] for g in sub)
+        if best is None or tot > best[0]:
+            best = (tot, sub)
+    chosen = []
+    for g in best[1]:
+        chosen += [g * epg + e for e in _rank_select(key[g * epg:(g + 1) * epg], per)]
+    order = _rank_select([key[e] if e in chosen else -math.inf for e in range(E)], k)
+    ssel = [s[e] for e in order]
+    return set(best[1]), order, [v / sum(ssel) * rsf for v in ssel]
+
+
+def test_vllm_grouped_matches_subset_enumeration():
+    rng = np.random.default_rng(12)
+    for trial in range(200):
+        n_group = int(rng.integers(1, 6))
+        epg = int(rng.integers(1, 7))
+        E = n_group * epg
+        topk_group = int(rng.integers(1, n_group + 1))
+        per = int(rng.integers(1, epg + 1))
+        k = per * topk_group
+        if trial % 3 == 0:   # exact ties in keys and group totals
+            logits = rng.integers(-2, 3, size=(1, E)).astype(np.float32)
+        else:
+            logits = rng.standard_normal((1, E)).astype(np.float32)
+        rsf = float(rng.choice([1.0, 2.5]))
+        chosen, sel, w = _vllm_grouped_brute(logits[0], n_group, topk_group, k, rsf)
+        ids, sc = oracle.route(logits, GROUPED_TOPK, k, n_group=n_group, topk_group=topk_group,
+                               routed_scaling_factor=rsf)
+        assert ids[0].tolist() == sel, (trial, ids, sel)
+        assert {e // epg for e in ids[0].tolist()} == chosen
+        for g in chosen:   # exactly k / topk_group experts from every kept group
+            assert sum(1 for e in ids[0].tolist() if e // epg == g) == per
+        np.testing.assert_allclose(sc[0], w, rtol=1e-12)
+        np.testing.assert_allclose(sc[0].sum(), rsf, rtol=1e-12)
+
+
+def test_vllm_grouped_reductions():
+    rng = np.random.default_rng(13)
+    logits = rng.standard_normal((64, 32)).astype(np.float32)
+    # one group: the per-group top-k is the plain top-k of the sigmoid scores
+    ia, sa = oracle.route(logits, GROUPED_TOPK, 4, n_group=1, topk_group=1)
+    ib, sb = oracle.route(logits, SIGMOID_RENORM, 4)
+    s = oracle.sigmoid64(logits.astype(np.float64)).astype(np.float32)
+    assert (np.take_along_axis(s, ia, 1) == np.take_along_axis(s, ib, 1)).all()
+    same = (ia == ib).all(1)
+    assert same.mean() > 0.9
+    np.testing.assert_allclose(sa[same], sb[same], rtol=1e-12)
+    # every expert of a kept group chosen: the kept groups are the top groups by total
+    ids, _ = oracle.route(logits, GROUPED_TOPK, 8, n_group=8, topk_group=2)
+    for t in range(64):
+        tot = [sum(float(v) for v in s[t, g * 4:(g + 1) * 4]) for g in range(8)]
+        top = sorted(range(8), key=lambda g: (-tot[g], g))[:2]
+        assert sorted(ids[t].tolist()) == sorted(e for g in top for e in range(4 * g, 4 * g + 4))
+    # softmax scoring is refused: its group totals are 1 in every group
+    with pytest.raises(ValueError, match="sums to 1"):
+        oracle.route(logits, GROUPED_TOPK_SOFTMAX, 4, n_group=8, topk_group=2)
+    with pytest.raises(ValueError):
+        oracle.route(logits, GROUPED_TOPK, 5, n_group=8, topk_group=2)   # 5 % 2 != 0
 
 
 def test_bias_moves_selection_not_weights():
