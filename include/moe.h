@@ -69,7 +69,15 @@ typedef enum {
   MOE_ROUTE_RENORMALIZE_NAIVE = 4, /* softmax over E -> top-k -> divide by the selected sum       */
   MOE_ROUTE_MINIMAX2 = 5,          /* sigmoid, +bias for selection, top-k over all E; weights =
                                       unbiased sigmoid / their sum (bias optional, NULL = 0)     */
-  MOE_ROUTE_SIGMOID_RENORM = 6     /* sigmoid -> top-k -> divide by the selected sum              */
+  MOE_ROUTE_SIGMOID_RENORM = 6,    /* sigmoid -> top-k -> divide by the selected sum              */
+  /* vLLM's GroupedTopKRouter (vLLM MoE page, section "GroupedTopKRouter：分组的专家选择"); the
+   * values lie outside RoutingMethodType's range (0-8). */
+  MOE_ROUTE_GROUPED_TOPK = 16,     /* sigmoid scores; group score = sum of the group's scores;
+                                      top topk_group groups; top_k / topk_group experts inside
+                                      each; weights = scores / their sum * rsf (see moe_route) */
+  MOE_ROUTE_GROUPED_TOPK_SOFTMAX = 17  /* the same with a softmax inside each group: its group
+                                      scores are all 1, so the group choice would rest on
+                                      tie-breaking alone; always rejected (MOE_REASON_DEGENERATE) */
 } moe_route_method;
 
 /* Why moe_can_implement rejected a problem. */
@@ -83,16 +91,17 @@ typedef enum {
   MOE_REASON_SHARED_I_ALIGN = 6,   /* shared_I < 0, shared_I % 64 != 0 or > 65536         */
   MOE_REASON_GROUPS = 7,           /* routing groups invalid (see moe_route)              */
   MOE_REASON_METHOD = 8,           /* unknown routing method                              */
-  MOE_REASON_ROWS = 9              /* T*k (+T shared) permuted rows reach 2^31             */
+  MOE_REASON_ROWS = 9,             /* T*k (+T shared) permuted rows reach 2^31             */
+  MOE_REASON_DEGENERATE = 10       /* a routing whose choice rests on tie-breaking alone   */
 } moe_reason;
 
 typedef struct {
   int32_t num_experts;            /* E                                                   */
   int32_t top_k;                  /* k                                                   */
   int32_t method;                 /* moe_route_method                                    */
-  int32_t n_group;                /* DeepSeekV3: expert groups (E % n_group == 0); else 1 */
-  int32_t topk_group;             /* DeepSeekV3: groups kept per token; else 1            */
-  float routed_scaling_factor;    /* DeepSeekV3: multiplies the weights; else ignored     */
+  int32_t n_group;                /* DeepSeekV3, GROUPED_TOPK: expert groups; else 1      */
+  int32_t topk_group;             /* DeepSeekV3, GROUPED_TOPK: groups kept; else 1        */
+  float routed_scaling_factor;    /* DeepSeekV3, GROUPED_TOPK: multiplies the weights     */
 } moe_route_params;
 
 typedef struct {
@@ -151,6 +160,13 @@ const char* moe_last_error(void);
  * 2 <= E/n_group <= 32, 1 <= topk_group <= n_group, k <= topk_group*E/n_group <= 256.
  * Outside it: MOE_ERR_UNSUPPORTED, nothing enqueued (there is no fallback).
  * Non-finite logits count as -inf for selection and in the normalisers.
+ * MOE_ROUTE_GROUPED_TOPK (vLLM MoE page, section "GroupedTopKRouter"): score
+ * s = sigmoid_fp64(l), key fl32(s); a group's score is the sum of its keys added in fp32
+ * in expert order; the topk_group best groups (ties to the lower group index), then the
+ * k / topk_group best keys inside each (ties to the lower index); slots by descending key;
+ * weights s / sum(s) * routed_scaling_factor. Needs E % n_group == 0, n_group <= 32,
+ * 1 <= topk_group <= n_group, k % topk_group == 0, k / topk_group <= E / n_group; `bias`
+ * must be NULL (MOE_ERR_INVALID_ARG otherwise).
  */
 moe_status moe_route(const float* logits, int64_t T, const float* bias, const moe_route_params* p,
                      int32_t* ids, float* scales, void* stream);

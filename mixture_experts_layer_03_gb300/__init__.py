@@ -20,8 +20,14 @@ LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
 MOE_ROUTE_DEFAULT = 0
 MOE_ROUTE_RENORMALIZE = 1
 MOE_ROUTE_DEEPSEEKV3 = 2
+MOE_ROUTE_LLAMA4 = 3
 MOE_ROUTE_RENORMALIZE_NAIVE = 4
+MOE_ROUTE_MINIMAX2 = 5
 MOE_ROUTE_SIGMOID_RENORM = 6
+MOE_ROUTE_GROUPED_TOPK = 16
+MOE_ROUTE_GROUPED_TOPK_SOFTMAX = 17
+
+MOE_REASON_DEGENERATE = 10
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1

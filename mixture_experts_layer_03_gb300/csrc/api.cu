@@ -53,6 +53,19 @@ int32_t route_reason(int64_t T, const moe_route_params& r) {
       if (epg * r.topk_group > 256 || r.top_k > epg * r.topk_group) return MOE_REASON_GROUPS;
       return MOE_REASON_OK;
     }
+    case MOE_ROUTE_GROUPED_TOPK: {
+      // vLLM GroupedTopKRouter: k / topk_group experts from each of topk_group groups. One
+      // warp lane scores each group, hence n_group <= 32.
+      if (r.n_group < 1 || r.n_group > 32 || r.num_experts % r.n_group != 0) return MOE_REASON_GROUPS;
+      if (r.topk_group < 1 || r.topk_group > r.n_group) return MOE_REASON_GROUPS;
+      if (r.top_k % r.topk_group != 0 || r.top_k / r.topk_group > r.num_experts / r.n_group)
+        return MOE_REASON_GROUPS;
+      return MOE_REASON_OK;
+    }
+    case MOE_ROUTE_GROUPED_TOPK_SOFTMAX:
+      // A softmax taken inside each group sums to 1 in every group: the group choice would
+      // be decided by tie-breaking alone.
+      return MOE_REASON_DEGENERATE;
     default:
       return MOE_REASON_METHOD;
   }
@@ -190,11 +203,16 @@ moe_status moe_route(const float* logits, int64_t T, const float* bias, const mo
                      int32_t* ids, float* scales, void* stream) {
   if (!p) return set_error(MOE_ERR_INVALID_ARG, "route params are NULL");
   const int32_t r = route_reason(T, *p);
+  if (r == MOE_REASON_DEGENERATE)
+    return set_error(MOE_ERR_UNSUPPORTED, "grouped top-k with softmax scoring: every group's score "
+                     "is 1, so the group choice would rest on tie-breaking alone");
   if (r != MOE_REASON_OK) return set_error(MOE_ERR_UNSUPPORTED, "routing outside the envelope (reason %d)", r);
   if (T == 0) return MOE_OK;
   if (!logits || !ids || !scales) return set_error(MOE_ERR_INVALID_ARG, "NULL logits/ids/scales");
   if (!aligned16(logits) || !aligned16(ids) || !aligned16(scales) || (bias && !aligned16(bias)))
     return set_error(MOE_ERR_INVALID_ARG, "route pointers must be 16-byte aligned");
+  if (bias && p->method == MOE_ROUTE_GROUPED_TOPK)
+    return set_error(MOE_ERR_INVALID_ARG, "the grouped top-k routing takes no bias");
   return launch_route(logits, T, bias, *p, ids, scales, static_cast<cudaStream_t>(stream));
 }
 

@@ -15,6 +15,11 @@
 //                    sum of the top-2 biased scores, keep topk_group groups, top-k among
 //                    their experts, weights = unbiased scores / (sum + 1e-20) * rsf.
 //
+//   GroupedTopK      vLLM's GroupedTopKRouter (vLLM MoE page, section "GroupedTopKRouter"),
+//                    sigmoid scoring: group score = sum of the group's scores, keep
+//                    topk_group groups, k / topk_group experts inside each, renormalise
+//                    (route_grouped_topk_kernel below).
+//
 // Selection keys are fp32 so ids are exact: the logit itself for the softmax and sigmoid
 // methods (both maps are increasing), and kappa = fl32(fl32(sigmoid_fp64(l)) + b) for
 // DeepSeekV3 and MiniMax2. Ties go to the lower expert index; slots are listed by
@@ -410,6 +415,177 @@ route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __
 }
 
 
+// vLLM grouped top-k with sigmoid scoring, one warp per token. The selection key of
+// expert e is fl32(sigmoid_fp64(l_e)); group g's score is the sum of its keys added in
+// fp32 in expert order (lane g adds them one by one); the topk_group best groups are
+// kept (ties: lower group index); inside each, its k / topk_group best keys (ties: lower
+// expert index). Slots are listed by descending key; weights = s / sum(s) * rsf with the
+// fp64 scores s of the chosen experts.
+//
+// Every key is first approximated in fp32 (1 / (1 + expf(-l)), within D of the exact key).
+// The decisions on approximate keys are accepted when each has a margin the error cannot
+// close: the last kept group's score beats the best dropped one by more than 2 Eg, where
+// Eg bounds a score's error (epg keys off by D each, plus one rounding of each partial
+// sum on either side: u * m per step, m <= epg the partial sum); and inside each kept
+// group the last chosen key beats the next by more than 2 D. Then the chosen set equals
+// the exact one; otherwise the token recomputes every key exactly and decides again. The
+// slot order and the weights always come from the exact keys and scores of the chosen k,
+// computed one per lane.
+template <int EPL>
+__device__ __forceinline__ bool grouped_topk_select(const float (&key)[EPL], const float* skey,
+                                                    int E, int n_group, int topk_group, int per,
+                                                    int lane, bool check, float D,
+                                                    int (&sel)[kMaxTopK]) {
+  const int epg = E / n_group;
+  float tot = -INFINITY;
+  if (lane < n_group) {
+    const float* gk = skey + lane * epg;
+    float acc = gk[0];
+    for (int j = 1; j < epg; ++j) acc = __fadd_rn(acc, gk[j]);
+    tot = acc;
+  }
+  bool certain = true;
+  // Groups: topk_group rounds of warp argmax (one more to read the best dropped score).
+  const float Eg = static_cast<float>(epg) * D + 6.0e-8f * static_cast<float>(epg) *
+                                                     static_cast<float>(epg + 1);
+  bool gtaken = false;
+  int groups[32];
+  float last = INFINITY;
+  for (int r = 0; r < topk_group; ++r) {
+    KeyIdx v = gtaken ? KeyIdx{-INFINITY, INT32_MAX} : KeyIdx{tot, lane < n_group ? lane : INT32_MAX};
+    v = warp_best(v);
+    if (v.idx == lane) gtaken = true;
+    groups[r] = v.idx;
+    last = v.key;
+  }
+  if (check && topk_group < n_group) {
+    KeyIdx v = gtaken ? KeyIdx{-INFINITY, INT32_MAX} : KeyIdx{tot, lane < n_group ? lane : INT32_MAX};
+    v = warp_best(v);
+    if (!(last - v.key > 2.0f * Eg)) certain = false;
+  }
+  // Experts: per rounds inside each kept group (one more for the margin).
+  int n = 0;
+  for (int r = 0; r < topk_group; ++r) {
+    const int lo = groups[r] * epg, hi = lo + epg;
+    uint32_t live = 0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e >= lo && e < hi) live |= 1u << i;
+    }
+    float kth = INFINITY;
+    for (int j = 0; j <= per; ++j) {
+      if (j == per && !check) break;
+      KeyIdx best{-INFINITY, INT32_MAX};
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if ((live >> i) & 1u && beats(key[i], e, best.key, best.idx)) {
+          best.key = key[i];
+          best.idx = e;
+        }
+      }
+      best = warp_best(best);
+      if (j < per) {
+        if ((best.idx & 31) == lane) live &= ~(1u << (best.idx >> 5));
+        // n < k <= kMaxTopK: every kept group contributes exactly per experts
+#pragma unroll
+        for (int q = 0; q < kMaxTopK; ++q)
+          if (q == n) sel[q] = best.idx;
+        ++n;
+        kth = best.key;
+      } else {
+        const float next = best.idx == INT32_MAX ? -INFINITY : best.key;
+        if (!(kth - next > 2.0f * D)) certain = false;
+      }
+    }
+  }
+  return certain;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+route_grouped_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int n_group,
+                          int topk_group, float rsf, int32_t* __restrict__ ids,
+                          float* __restrict__ scales) {
+  __shared__ float s_key[kRouteWarps][256];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp;
+  pdl_trigger();
+  pdl_wait();
+  if (t >= T) return;   // warp-uniform; the kernel has no block-wide barrier
+
+  const float* row = logits + t * E;
+  float l[EPL], key[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    float v = -INFINITY;
+    key[i] = -INFINITY;
+    if (e < E) {
+      v = row[e];
+      if (!isfinite(v)) v = -INFINITY;
+      key[i] = v == -INFINITY ? 0.0f : 1.0f / (1.0f + expf(-v));   // sigmoid(-inf) = 0 exactly
+      s_key[warp][e] = key[i];
+    }
+    l[i] = v;
+  }
+  __syncwarp();
+  // The fp32 sigmoid is within a few ulp of the true value (keys lie in [0, 1]) and the
+  // exact key adds one rounding: 1.25e-6 bounds the difference with a wide margin.
+  constexpr float D = 1.25e-6f;
+  const int per = k / topk_group;
+  int sel[kMaxTopK];
+  bool certain = grouped_topk_select(key, s_key[warp], E, n_group, topk_group, per, lane, true, D, sel);
+  if (!certain) {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        key[i] = l[i] == -INFINITY ? 0.0f : __double2float_rn(sigmoid_d(static_cast<double>(l[i])));
+        s_key[warp][e] = key[i];
+      }
+    }
+    __syncwarp();
+    grouped_topk_select(key, s_key[warp], E, n_group, topk_group, per, lane, false, 0.0f, sel);
+  }
+
+  // Lane j < k: the j-th chosen expert's exact score and key; its slot is the number of
+  // chosen experts that beat it (larger key, or the same key and a lower index).
+  int me = INT32_MAX;
+#pragma unroll
+  for (int q = 0; q < kMaxTopK; ++q)
+    if (q < k && q == lane) me = sel[q];
+  double s = 0.0;
+  float ek = -INFINITY;
+  if (lane < k) {
+    const float v = row[me];
+    s = isfinite(v) ? sigmoid_d(static_cast<double>(v)) : 0.0;   // non-finite counts as -inf
+    ek = __double2float_rn(s);
+  }
+  int slot = 0;
+  for (int q = 0; q < k; ++q) {
+    const float ok = __shfl_sync(0xffffffffu, ek, q);
+    const int oe = __shfl_sync(0xffffffffu, me, q);
+    if (q != lane && beats(ok, oe, ek, me)) ++slot;
+  }
+  const double sum = warp_sum_d(s);
+  if (lane < k) {
+    ids[t * k + slot] = me;
+    scales[t * k + slot] = __double2float_rn(s / sum * static_cast<double>(rsf));
+  }
+}
+
+template <int EPL>
+cudaError_t launch_grouped_topk_t(const float* logits, int64_t T, const moe_route_params& p,
+                                  int32_t* ids, float* scales, cudaStream_t s) {
+  const int64_t blocks = (T + kRouteWarps - 1) / kRouteWarps;
+  return launch_pdl(route_grouped_topk_kernel<EPL>, dim3(static_cast<unsigned>(blocks)),
+                    dim3(kRouteWarps * 32), 0, s, logits, T, p.num_experts, p.top_k, p.n_group,
+                    p.topk_group, p.routed_scaling_factor, ids, scales);
+}
+
 template <int EPL, bool kGrouped>
 cudaError_t launch_route_t(const float* logits, int64_t T, const float* bias,
                            const moe_route_params& p, int32_t* ids, float* scales, cudaStream_t s) {
@@ -439,8 +615,17 @@ moe_status launch_route(const float* logits, int64_t T, const float* bias,
                         cudaStream_t s) {
   if (T == 0) return MOE_OK;
   const bool keyed = p.method == MOE_ROUTE_DEEPSEEKV3 || p.method == MOE_ROUTE_MINIMAX2;
-  const cudaError_t err = keyed ? launch_route_e<true>(logits, T, bias, p, ids, scales, s)
-                                : launch_route_e<false>(logits, T, bias, p, ids, scales, s);
+  cudaError_t err;
+  if (p.method == MOE_ROUTE_GROUPED_TOPK) {
+    const int E = p.num_experts;
+    err = E <= 32    ? launch_grouped_topk_t<1>(logits, T, p, ids, scales, s)
+          : E <= 64  ? launch_grouped_topk_t<2>(logits, T, p, ids, scales, s)
+          : E <= 128 ? launch_grouped_topk_t<4>(logits, T, p, ids, scales, s)
+                     : launch_grouped_topk_t<8>(logits, T, p, ids, scales, s);
+  } else {
+    err = keyed ? launch_route_e<true>(logits, T, bias, p, ids, scales, s)
+                : launch_route_e<false>(logits, T, bias, p, ids, scales, s);
+  }
   if (err != cudaSuccess)
     return set_error(MOE_ERR_CUDA, "route_kernel launch: %s", cudaGetErrorString(err));
   return MOE_OK;

@@ -104,6 +104,12 @@ def _route_params(moe, E, k, method, n_group=1, topk_group=1, rsf=1.0):
     (64, 8, 2, 1, 1, False),   # 64 experts in one group > 32 per group
     (8, 8, 2, 4, 2, False),    # k > topk_group * experts per group
     (8, 4, 2, 4, 2, True), (8, 2, 2, 8, 2, False),   # one expert per group: no top-2
+    # vLLM grouped top-k: k / topk_group experts from each kept group
+    (256, 8, 16, 8, 4, True), (32, 8, 16, 32, 8, True), (256, 8, 16, 1, 1, True),
+    (256, 6, 16, 8, 4, False),   # 6 % 4 != 0
+    (16, 8, 16, 8, 2, False),    # 4 per group > 2 experts per group
+    (256, 8, 16, 64, 8, False),  # more than 32 groups
+    (96, 4, 16, 5, 2, False),    # 96 % 5 != 0
 ])
 def test_route_envelope_is_checked_on_the_host(moe, E, k, method, ng, tg, ok):
     """T = 0 enqueues nothing; an unsupported configuration is rejected synchronously."""
@@ -112,6 +118,17 @@ def test_route_envelope_is_checked_on_the_host(moe, E, k, method, ng, tg, ok):
     assert (st == moe.MOE_OK) == ok, moe._lib.moe_last_error()
     if not ok:
         assert st == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_grouped_topk_softmax_is_refused_and_bias_rejected(moe):
+    p = _route_params(moe, 256, 8, moe.MOE_ROUTE_GROUPED_TOPK_SOFTMAX, 8, 4)
+    st = moe._lib.moe_route(None, 0, None, ctypes.byref(p), None, None, None)
+    assert st == moe.MOE_ERR_UNSUPPORTED
+    assert b"tie-breaking" in moe._lib.moe_last_error()
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: the bias check comes first
+    p = _route_params(moe, 256, 8, moe.MOE_ROUTE_GROUPED_TOPK, 8, 4)
+    st = moe._lib.moe_route(fake, 4, fake, ctypes.byref(p), fake, fake, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
 
 
 def test_forward_host_errors(moe):

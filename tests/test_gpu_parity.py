@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from workloads import (WORKLOADS, Workload, make_inputs, DEFAULT, RENORMALIZE, DEEPSEEKV3,
-                       LLAMA4, RENORMALIZE_NAIVE, MINIMAX2, SIGMOID_RENORM)
+                       LLAMA4, RENORMALIZE_NAIVE, MINIMAX2, SIGMOID_RENORM, GROUPED_TOPK)
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
@@ -75,6 +75,12 @@ ROUTE_CASES = [
     (257, 256, 8, MINIMAX2, 1, 1, 1.0, 1.0, False),           # biased keys over all 256
     (100, 64, 4, MINIMAX2, 1, 1, 1.0, 1.0, False),
     (64, 16, 4, MINIMAX2, 1, 1, 1.0, 1.0, True),              # ties in the keys
+    (257, 256, 8, GROUPED_TOPK, 8, 4, 2.5, 1.0, False),       # vLLM grouped: 2 from 4 of 8 groups
+    (100, 64, 6, GROUPED_TOPK, 8, 3, 1.0, 1.0, False),
+    (64, 16, 4, GROUPED_TOPK, 4, 2, 1.0, 1.0, True),          # ties in keys and group totals
+    (100, 96, 4, GROUPED_TOPK, 1, 1, 1.0, 1.0, False),        # one group of 96
+    (100, 32, 8, GROUPED_TOPK, 32, 8, 1.0, 1.0, False),       # one expert per group
+    (100, 128, 8, GROUPED_TOPK, 16, 2, 1.0, 3.0, False),      # 4 from 2 of 16 groups
 ]
 
 
@@ -96,7 +102,8 @@ def test_route_parity(moe, case):
     np.testing.assert_allclose(sc.cpu().numpy(), sc_ref, rtol=1e-6, atol=0)
 
 
-@pytest.mark.parametrize("method,E,ng,tg", [(DEEPSEEKV3, 256, 8, 4), (MINIMAX2, 128, 1, 1)])
+@pytest.mark.parametrize("method,E,ng,tg", [(DEEPSEEKV3, 256, 8, 4), (MINIMAX2, 128, 1, 1),
+                                            (GROUPED_TOPK, 256, 8, 4)])
 def test_route_near_ties_in_biased_keys(moe, method, E, ng, tg):
     """Keys that differ by about one fp32 ulp, where the fp32 approximation of the keys
     cannot decide the order: the ids must still match the exact-key oracle."""
@@ -105,9 +112,11 @@ def test_route_near_ties_in_biased_keys(moe, method, E, ng, tg):
     logits = torch.randn(T, E, generator=g)
     # every other expert gets the next fp32 logit above its neighbour's
     logits[:, 1::2] = torch.nextafter(logits[:, 0::2], torch.full_like(logits[:, 0::2], 10.0))
-    bias = torch.zeros(E)
-    ids, sc = moe.moe_route(logits.cuda(), method, 8, bias=bias.cuda(), n_group=ng, topk_group=tg)
-    ids_ref, sc_ref = oracle.route(logits.numpy(), method, 8, bias=bias.numpy(), n_group=ng,
+    bias = None if method == GROUPED_TOPK else torch.zeros(E)
+    ids, sc = moe.moe_route(logits.cuda(), method, 8, bias=None if bias is None else bias.cuda(),
+                            n_group=ng, topk_group=tg)
+    ids_ref, sc_ref = oracle.route(logits.numpy(), method, 8,
+                                   bias=None if bias is None else bias.numpy(), n_group=ng,
                                    topk_group=tg)
     assert np.array_equal(ids.cpu().numpy(), ids_ref)
     np.testing.assert_allclose(sc.cpu().numpy(), sc_ref, rtol=1e-6, atol=0)

@@ -34,6 +34,9 @@ LLAMA4 = 3
 RENORMALIZE_NAIVE = 4
 MINIMAX2 = 5
 SIGMOID_RENORM = 6
+# vLLM's GroupedTopKRouter with sigmoid scoring (vLLM MoE page, section "GroupedTopKRouter");
+# a code outside the RoutingMethodType range.
+GROUPED_TOPK = 16
 
 
 @dataclasses.dataclass(frozen=True)
@@ -159,4 +162,4 @@ def min_bytes(w: Workload, n_active: int) -> float:
 
 __all__ = ["Workload", "WORKLOADS", "ORDER", "make_inputs", "small_case", "zipf_logit_bias",
            "flops", "min_bytes", "DEFAULT", "RENORMALIZE", "DEEPSEEKV3", "LLAMA4",
-           "RENORMALIZE_NAIVE", "MINIMAX2", "SIGMOID_RENORM"]
+           "RENORMALIZE_NAIVE", "MINIMAX2", "SIGMOID_RENORM", "GROUPED_TOPK"]
