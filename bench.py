@@ -442,6 +442,35 @@ def measure(name: str, args, rank: int, world: int, dev, headline: bool) -> dict
                 "unit": "TFLOP/s" if g_tc else "GB/s"}
         gate["frac"] = round(gate["achieved"] / (peaks["bf16_tflops"] if g_tc else
                                                 peaks["hbm_gbs"]), 4)
+        # The gate with this workload's routing fused into its epilogue (moe_gate_route, no
+        # logits written), against the gate and the route kernel launched one after the other.
+        rkw = dict(bias=bias, n_group=w.n_group, topk_group=w.topk_group,
+                   routed_scaling_factor=w.rsf)
+        ids_g, sc_g = torch.empty_like(ids), torch.empty_like(sc)
+        ids_s, sc_s = torch.empty_like(ids), torch.empty_like(sc)
+        for _ in range(3):
+            moe.moe_gate_route(x, wg, w.method, w.k, w.E, ids=ids_g, scales=sc_g,
+                               shared_logits=sg_g, stream=stream, **rkw)
+        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(20_000_000)
+        for i in range(reps):
+            flush(i)
+            fev[i][0].record(stream)
+            moe.moe_gate_route(x, wg, w.method, w.k, w.E, ids=ids_g, scales=sc_g,
+                               shared_logits=sg_g, stream=stream, **rkw)
+            fev[i][1].record(stream)
+            flush(i)
+            fev[i][2].record(stream)
+            moe.moe_gate(x, wg, w.E, lg_g, sg_g, stream=stream)
+            moe.moe_route(lg_g, w.method, w.k, ids=ids_s, scales=sc_s, stream=stream, **rkw)
+            fev[i][3].record(stream)
+        torch.cuda.synchronize()
+        gate["gate_route_fused_ms"] = round(statistics.median(
+            fev[i][0].elapsed_time(fev[i][1]) for i in range(reps)), 4)
+        gate["gate_then_route_ms"] = round(statistics.median(
+            fev[i][2].elapsed_time(fev[i][3]) for i in range(reps)), 4)
+        gate["fused_same_ids"] = bool(torch.equal(ids_g, ids_s))
 
     # ---- end to end through the public API: every step copies its inputs (x, logits)
     # in from pinned host memory and its result (y) out to pinned host memory. Three

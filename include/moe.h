@@ -249,6 +249,24 @@ moe_status moe_static_read_device_status(void* stream, int32_t* flags);
 moe_status moe_gate(const void* x, const void* wg, int64_t T, int32_t H, int32_t E,
                     int32_t n_shared, float* routed_logits, float* shared_logits, void* stream);
 
+/* Router gate and routing in one launch (vLLM MoE page, section "Gate 计算与 FSE": the gate
+ * GEMM that produces router_logits; TensorRT-LLM MoE page, layer-structure figure: fc_gate
+ * ahead of routing): moe_gate, then moe_route on its logits. After the gate's fixed-order
+ * reduction, the CTA that holds a token's complete row of routed logits routes the token
+ * itself, so the logits need not travel through HBM to a second launch.
+ *   x, wg, T, H, n_shared  as for moe_gate, with E = p->num_experts
+ *   bias, p                as for moe_route (every method and envelope of moe_route)
+ *   ids, scales            device int32 / fp32 [T, k] out, as moe_route writes them
+ *   routed_logits          device fp32 [T, E] out, or NULL (then not written)
+ *   shared_logits          device fp32 [T] out when n_shared = 1, else ignored (may be NULL)
+ * The logits equal moe_gate's and the ids and scales equal moe_route's on those logits, bit
+ * for bit. Errors: those of moe_gate and of moe_route, checked on the host before anything
+ * is enqueued. */
+moe_status moe_gate_route(const void* x, const void* wg, int64_t T, int32_t H, int32_t n_shared,
+                          const float* bias, const moe_route_params* p, int32_t* ids,
+                          float* scales, float* routed_logits, float* shared_logits,
+                          void* stream);
+
 /* moe_forward restricted to the experts [e_lo, e_hi) of this call: the expert-parallel
  * seam of the TensorRT-LLM MoE page, section on supports_finalize_before_combine ("finalize
  * before combine": the top-k weighted sum taken on a rank's own rows, slots of other

@@ -80,6 +80,8 @@ _SIGS = {
                                            _P, ctypes.c_size_t, _P]),
     "moe_gate": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                 ctypes.c_int32, _P, _P, _P]),
+    "moe_gate_route": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P,
+                                      ctypes.POINTER(MoeRouteParams), _P, _P, _P, _P, _P]),
     "moe_permute": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_fc1": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_fc2": (ctypes.c_int, [ctypes.POINTER(MoeProblem), _P, _P, _P, ctypes.c_size_t, _P]),
@@ -284,6 +286,40 @@ def moe_gate(x, wg, num_experts: int, routed_logits=None, shared_logits=None, st
     _check(_lib.moe_gate(_ptr(x), _ptr(wg), T, H, E, n_shared, _ptr(routed_logits),
                          _ptr(shared_logits) if n_shared else None, _stream(stream)), "moe_gate")
     return routed_logits, (shared_logits if n_shared else None)
+
+
+def moe_gate_route(x, wg, method: int, top_k: int, num_experts: int,
+                   bias: Optional[torch.Tensor] = None, n_group: int = 1, topk_group: int = 1,
+                   routed_scaling_factor: float = 1.0, ids=None, scales=None,
+                   routed_logits=None, shared_logits=None, want_logits: bool = False,
+                   stream=None):
+    """Router gate and routing in one launch: x bf16 [T, H], wg bf16 [E (+1), H] ->
+    (ids int32 [T, k], scales fp32 [T, k], routed logits fp32 [T, E] or None, shared-expert
+    gate logits fp32 [T] or None). The routed logits are written only when want_logits is
+    set or routed_logits is passed."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(wg, "wg", torch.bfloat16)
+    T, H = x.shape
+    E = int(num_experts)
+    n_shared = wg.shape[0] - E
+    if n_shared not in (0, 1) or wg.shape[1] != H:
+        raise ValueError(f"wg must be [{E} or {E + 1}, {H}], got {tuple(wg.shape)}")
+    if bias is not None:
+        _cuda(bias, "bias", torch.float32)
+    if ids is None:
+        ids = torch.empty((T, top_k), dtype=torch.int32, device=x.device)
+    if scales is None:
+        scales = torch.empty((T, top_k), dtype=torch.float32, device=x.device)
+    if want_logits and routed_logits is None:
+        routed_logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    if n_shared and shared_logits is None:
+        shared_logits = torch.empty((T,), dtype=torch.float32, device=x.device)
+    p = MoeRouteParams(E, top_k, method, n_group, topk_group, routed_scaling_factor)
+    _check(_lib.moe_gate_route(_ptr(x), _ptr(wg), T, H, n_shared, _ptr(bias), ctypes.byref(p),
+                               _ptr(ids), _ptr(scales), _ptr(routed_logits),
+                               _ptr(shared_logits) if n_shared else None, _stream(stream)),
+           "moe_gate_route")
+    return ids, scales, routed_logits, (shared_logits if n_shared else None)
 
 
 MOE_STATIC_SCRATCH_BYTES = 32 << 20

@@ -289,6 +289,39 @@ moe_status moe_gate(const void* x, const void* wg, int64_t T, int32_t H, int32_t
                      nullptr, static_cast<cudaStream_t>(stream));
 }
 
+moe_status moe_gate_route(const void* x, const void* wg, int64_t T, int32_t H, int32_t n_shared,
+                          const float* bias, const moe_route_params* p, int32_t* ids,
+                          float* scales, float* routed_logits, float* shared_logits,
+                          void* stream) {
+  if (!p) return set_error(MOE_ERR_INVALID_ARG, "route params are NULL");
+  const int32_t E = p->num_experts;
+  if (T < 0 || T > (int64_t{1} << 31) / 8 || H < 64 || H % 64 != 0 || H > 32768 || E < 1 ||
+      E > 256 || n_shared < 0 || n_shared > 1)
+    return set_error(MOE_ERR_UNSUPPORTED, "gate shape outside the envelope (T %lld, H %d, E %d, "
+                     "n_shared %d)", static_cast<long long>(T), H, E, n_shared);
+  const int32_t r = route_reason(T, *p);
+  if (r == MOE_REASON_DEGENERATE)
+    return set_error(MOE_ERR_UNSUPPORTED, "grouped top-k with softmax scoring: every group's score "
+                     "is 1, so the group choice would rest on tie-breaking alone");
+  if (r != MOE_REASON_OK) return set_error(MOE_ERR_UNSUPPORTED, "routing outside the envelope (reason %d)", r);
+  if (T == 0) return MOE_OK;
+  if (!x || !wg || !ids || !scales || (n_shared == 1 && !shared_logits))
+    return set_error(MOE_ERR_INVALID_ARG, "NULL gate or routing argument");
+  if (!aligned16(x) || !aligned16(wg) || !aligned16(ids) || !aligned16(scales) ||
+      (routed_logits && !aligned16(routed_logits)) || (shared_logits && !aligned16(shared_logits)) ||
+      (bias && !aligned16(bias)))
+    return set_error(MOE_ERR_INVALID_ARG, "gate and routing pointers must be 16-byte aligned");
+  if (bias && p->method == MOE_ROUTE_GROUPED_TOPK)
+    return set_error(MOE_ERR_INVALID_ARG, "the grouped top-k routing takes no bias");
+  GateRouteArgs ra;
+  ra.params = *p;
+  ra.bias = bias;
+  ra.ids = ids;
+  ra.scales = scales;
+  return launch_gate(x, wg, T, H, E, n_shared, routed_logits, n_shared ? shared_logits : nullptr,
+                     nullptr, static_cast<cudaStream_t>(stream), &ra);
+}
+
 moe_status moe_forward_partial(const moe_problem* p, int32_t e_lo, int32_t e_hi, const void* x,
                                const int32_t* ids, const float* scales, const void* w13,
                                const void* w2, const void* w13_s, const void* w2_s,

@@ -10,6 +10,11 @@
 // (read through distributed shared memory) in rank order, so the sums are deterministic.
 // Rows past T and columns past E + n_shared are zero-filled by the tensor maps and not
 // stored.
+//
+// Gate with routing (moe_gate_route): after the reduction each CTA holds its rows' complete
+// routed logits (all E <= 256 routed columns lie in column tile 0) in shared memory, and
+// its warps route those tokens there (one warp per token, the selection and weights of
+// route_device.cuh), so the logits need not go through HBM to a second launch.
 #include <atomic>
 #include <cstdint>
 
@@ -19,6 +24,7 @@
 #include "internal.h"
 #include "launch.cuh"
 #include "ptx.cuh"
+#include "route_device.cuh"
 #include "tmap.cuh"
 
 namespace moe {
@@ -32,6 +38,15 @@ constexpr int kGateWMaxBytes = 256 * kGateRowBytes;    // up to 256 gate rows
 constexpr int kGateRingBytes = 4 * (kGateXBytes + kGateWMaxBytes);   // 192 KB of stages
 constexpr int kGateSmemBytes = 1024 + kGateRingBytes;
 constexpr int kGateMaxSplit = 8;             // portable cluster size
+// Routing scratch of the fused gate + route kernel, inside the (by then idle) stage ring,
+// past the partial tile (at most 128 rows x 260 floats = 130 KB): per warp 256 keys and
+// 256 exact-key flags.
+constexpr int kGateRouteScratch = 136 * 1024;
+static_assert(kGateRouteScratch >= 128 * (256 + 4) * 4, "routing scratch overlaps the partial tile");
+static_assert(kGateRouteScratch + 4 * (256 * 4 + 256) <= kGateRingBytes, "routing scratch past the ring");
+
+// Routing done in the fused kernel's epilogue.
+enum GateRoute { kGateNoRoute = 0, kGateRoutePlain = 1, kGateRouteKeyed = 2, kGateRouteGroupedTopk = 3 };
 static_assert(kGateBK == static_cast<int>(kMapBoxCols), "tensor-map boxes are one K block wide");
 
 struct GateArgs {
@@ -45,11 +60,19 @@ struct GateArgs {
   int stage_bytes;  // X box + W box, rounded up to 1024 (the swizzle atom)
   int stages;       // ring depth: as many stages as fit in the ring, at most 8
   uint32_t tmem_cols;
-  float* logits;          // [T, E]
+  float* logits;          // [T, E], or NULL (fused routing without the logits written)
   float* shared_logits;   // [T] or NULL
   int32_t* status;        // device status word or NULL
+  // routing (fused kernel only)
+  int method, k, n_group, topk_group;
+  float rsf;
+  const float* bias;      // [E] or NULL
+  int32_t* ids;           // [T, k]
+  float* scales;          // [T, k]
 };
 
+// kRoute: GateRoute; EPL: routed experts per lane of the routing warps (E <= 32 * EPL).
+template <int EPL, int kRoute>
 __global__ void __launch_bounds__(128, 1)
 gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
             GateArgs g) {
@@ -189,9 +212,44 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
       for (int j = 0; j < 4; ++j) {
         const int c = col0 + col + j;
         if (col + j >= n_cols) break;
-        if (c < g.E) g.logits[t * g.E + c] = sum[j];
-        else if (g.shared_logits) g.shared_logits[t] = sum[j];
+        if (c < g.E) {
+          if (kRoute == kGateNoRoute || g.logits) g.logits[t * g.E + c] = sum[j];
+        } else if (g.shared_logits) {
+          g.shared_logits[t] = sum[j];
+        }
       }
+    }
+    if (kRoute != kGateNoRoute) {
+      // The reduced row replaces this CTA's own partial in place: rows [r0, r1) of this
+      // CTA's tile are read by this thread only (the other CTAs reduce other rows).
+      float* dst = partial + row * pstride + col;
+      dst[0] = sum[0];
+      dst[1] = sum[1];
+      dst[2] = sum[2];
+      dst[3] = sum[3];
+    }
+  }
+  if (kRoute != kGateNoRoute && col_tile == 0) {
+    // Route this CTA's tokens on their reduced logits (columns 0..E-1 of the rows).
+    __syncthreads();
+    float* skey = reinterpret_cast<float*>(smem + kGateRouteScratch) + warp * 256;
+    uint8_t* sexact = smem + kGateRouteScratch + 4 * 256 * 4 + warp * 256;
+    for (int row = r0 + warp; row < r1; row += 4) {
+      const int64_t t = row0 + row;
+      if (t >= g.T) break;
+      const float* lrow = partial + row * pstride;
+      if (kRoute == kGateRouteGroupedTopk) {
+        grouped_topk_token<EPL>(lrow, g.E, g.k, g.n_group, g.topk_group, g.rsf, lane, skey,
+                                g.ids + t * g.k, g.scales + t * g.k);
+      } else {
+        int sel[kMaxTopK];
+        double z = 0.0;
+        select_token<EPL, kRoute == kGateRouteKeyed>(lrow, g.E, g.bias, g.method, g.k, g.n_group,
+                                                     g.topk_group, lane, skey, sexact, sel, &z);
+        token_weights_warp<kRoute == kGateRouteKeyed>(lrow, sel, g.k, g.method, z, g.rsf, lane,
+                                                      g.ids + t * g.k, g.scales + t * g.k);
+      }
+      __syncwarp();
     }
   }
   cluster_sync();   // no CTA leaves while another reads its shared memory
@@ -203,21 +261,43 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
   }
 }
 
+// The dynamic shared-memory opt-in of one instantiation, once per device (published after
+// it is set; a thread that finds it unset sets it again, which is harmless).
+template <int EPL, int kRoute>
+cudaError_t gate_smem_optin() {
+  static std::atomic<bool> done[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(gate_kernel<EPL, kRoute>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kGateSmemBytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
+template <int EPL, int kRoute>
+cudaError_t launch_gate_t(const cudaLaunchConfig_t& cfg, const CUtensorMap& mx,
+                          const CUtensorMap& mw, const GateArgs& g) {
+  const cudaError_t e = gate_smem_optin<EPL, kRoute>();
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, gate_kernel<EPL, kRoute>, mx, mw, g);
+}
+
+template <int kRoute>
+cudaError_t launch_gate_e(const cudaLaunchConfig_t& cfg, const CUtensorMap& mx,
+                          const CUtensorMap& mw, const GateArgs& g) {
+  if (g.E <= 32) return launch_gate_t<1, kRoute>(cfg, mx, mw, g);
+  if (g.E <= 64) return launch_gate_t<2, kRoute>(cfg, mx, mw, g);
+  if (g.E <= 128) return launch_gate_t<4, kRoute>(cfg, mx, mw, g);
+  return launch_gate_t<8, kRoute>(cfg, mx, mw, g);
+}
+
 }  // namespace
 
 moe_status launch_gate(const void* x, const void* wg, int64_t T, int H, int E, int n_shared,
-                       float* logits, float* shared_logits, int32_t* status, cudaStream_t s) {
-  // The shared-memory opt-in, once per device (published after it is set; a thread that
-  // finds it unset sets it again, which is harmless).
-  static std::atomic<bool> attr_done[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_acquire)) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGateSmemBytes);
-    if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "gate smem attribute: %s", cudaGetErrorString(e));
-    if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
-  }
+                       float* logits, float* shared_logits, int32_t* status, cudaStream_t s,
+                       const GateRouteArgs* route) {
   GateArgs g;
   g.T = T;
   g.H = H;
@@ -243,6 +323,32 @@ moe_status launch_gate(const void* x, const void* wg, int64_t T, int H, int E, i
   g.logits = logits;
   g.shared_logits = shared_logits;
   g.status = status;
+  g.method = 0;
+  g.k = 0;
+  g.n_group = 1;
+  g.topk_group = 1;
+  g.rsf = 1.0f;
+  g.bias = nullptr;
+  g.ids = nullptr;
+  g.scales = nullptr;
+  int mode = kGateNoRoute;
+  if (route) {
+    const moe_route_params& p = route->params;
+    const bool keyed = p.method == MOE_ROUTE_DEEPSEEKV3 || p.method == MOE_ROUTE_MINIMAX2;
+    const bool dsv3 = p.method == MOE_ROUTE_DEEPSEEKV3;
+    const bool vgrp = p.method == MOE_ROUTE_GROUPED_TOPK;
+    mode = vgrp ? kGateRouteGroupedTopk : keyed ? kGateRouteKeyed : kGateRoutePlain;
+    g.method = p.method;
+    g.k = p.top_k;
+    // as in moe_route: groups and the scaling factor belong to DeepSeekV3 and the grouped
+    // top-k; MiniMax2 has one group and its bias is optional
+    g.n_group = (dsv3 || vgrp) ? p.n_group : 1;
+    g.topk_group = (dsv3 || vgrp) ? p.topk_group : 1;
+    g.rsf = (dsv3 || vgrp) ? p.routed_scaling_factor : 1.0f;
+    g.bias = keyed ? route->bias : nullptr;
+    g.ids = route->ids;
+    g.scales = route->scales;
+  }
   CUtensorMap mx, mw;
   if (!encode_map2(&mx, x, static_cast<uint64_t>(T), static_cast<uint64_t>(H), 128) ||
       !encode_map2(&mw, wg, static_cast<uint64_t>(g.E_out), static_cast<uint64_t>(H),
@@ -262,7 +368,13 @@ moe_status launch_gate(const void* x, const void* wg, int64_t T, int H, int E, i
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t err = cudaLaunchKernelEx(&cfg, gate_kernel, mx, mw, g);
+  cudaError_t err;
+  switch (mode) {
+    case kGateRoutePlain: err = launch_gate_e<kGateRoutePlain>(cfg, mx, mw, g); break;
+    case kGateRouteKeyed: err = launch_gate_e<kGateRouteKeyed>(cfg, mx, mw, g); break;
+    case kGateRouteGroupedTopk: err = launch_gate_e<kGateRouteGroupedTopk>(cfg, mx, mw, g); break;
+    default: err = launch_gate_t<1, kGateNoRoute>(cfg, mx, mw, g); break;
+  }
   if (err != cudaSuccess) return set_error(MOE_ERR_CUDA, "gate launch: %s", cudaGetErrorString(err));
   return MOE_OK;
 }

@@ -92,8 +92,18 @@ moe_status launch_finalize(const moe_problem& p, const moe_ws_layout& L, const f
 // Device failure-path self-test (selftest.cu): status = the workspace status words.
 moe_status launch_wait_selftest(int32_t* status, cudaStream_t s);
 
+// Routing fused into the gate's epilogue (moe_gate_route); arguments as for moe_route.
+struct GateRouteArgs {
+  moe_route_params params;
+  const float* bias;
+  int32_t* ids;
+  float* scales;
+};
+
+// logits may be NULL when `route` is given (the routed logits are then not written).
 moe_status launch_gate(const void* x, const void* wg, int64_t T, int H, int E, int n_shared,
-                       float* logits, float* shared_logits, int32_t* status, cudaStream_t s);
+                       float* logits, float* shared_logits, int32_t* status, cudaStream_t s,
+                       const GateRouteArgs* route = nullptr);
 
 moe_status launch_cast_f32_bf16(const float* in, void* out, int64_t n, cudaStream_t s);
 

@@ -131,6 +131,34 @@ def test_grouped_topk_softmax_is_refused_and_bias_rejected(moe):
     assert st == moe.MOE_ERR_INVALID_ARG
 
 
+def test_gate_route_host_errors(moe):
+    lib = moe._lib
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails on the host
+    p = _route_params(moe, 8, 2, 4)
+    # T = 0 is a no-op
+    assert lib.moe_gate_route(None, None, 0, 128, 0, None, ctypes.byref(p), None, None, None, None,
+                              None) == moe.MOE_OK
+    # H not a multiple of 64, E too large, bad routing
+    assert lib.moe_gate_route(fake, fake, 4, 100, 0, None, ctypes.byref(p), fake, fake, None, None,
+                              None) == moe.MOE_ERR_UNSUPPORTED
+    big = _route_params(moe, 300, 2, 4)
+    assert lib.moe_gate_route(fake, fake, 4, 128, 0, None, ctypes.byref(big), fake, fake, None,
+                              None, None) == moe.MOE_ERR_UNSUPPORTED
+    soft = _route_params(moe, 256, 8, moe.MOE_ROUTE_GROUPED_TOPK_SOFTMAX, 8, 4)
+    assert lib.moe_gate_route(fake, fake, 4, 128, 0, None, ctypes.byref(soft), fake, fake, None,
+                              None, None) == moe.MOE_ERR_UNSUPPORTED
+    # missing outputs, misaligned pointers, a shared gate row without its output
+    assert lib.moe_gate_route(fake, fake, 4, 128, 0, None, ctypes.byref(p), None, fake, None, None,
+                              None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_gate_route(ctypes.c_void_p((1 << 20) + 4), fake, 4, 128, 0, None,
+                              ctypes.byref(p), fake, fake, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_gate_route(fake, fake, 4, 128, 1, None, ctypes.byref(p), fake, fake, None, None,
+                              None) == moe.MOE_ERR_INVALID_ARG
+    gt = _route_params(moe, 256, 8, moe.MOE_ROUTE_GROUPED_TOPK, 8, 4)
+    assert lib.moe_gate_route(fake, fake, 4, 128, 0, fake, ctypes.byref(gt), fake, fake, None, None,
+                              None) == moe.MOE_ERR_INVALID_ARG
+
+
 def test_forward_host_errors(moe):
     p = moe.make_problem(T=16, H=128, I=64, E=4, k=2)
     n = moe.moe_workspace_bytes(p)

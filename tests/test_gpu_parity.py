@@ -383,6 +383,61 @@ def test_gate_parity_and_routing_on_its_logits(moe, T, H, E, ns, method):
     np.testing.assert_allclose(sc.cpu().numpy(), sc_ref, rtol=1e-6, atol=0)
 
 
+GATE_ROUTE_CASES = [
+    # T, H, E, n_shared, method, k, routing kwargs, integer-valued inputs (exact ties)
+    (300, 256, 8, 0, RENORMALIZE_NAIVE, 2, {}, False),
+    (513, 1024, 256, 1, DEEPSEEKV3, 8, dict(n_group=8, topk_group=4, routed_scaling_factor=2.5),
+     False),                                                   # FSE row in a second column tile
+    (64, 2048, 128, 0, RENORMALIZE_NAIVE, 8, {}, False),       # decode: the gate split along K
+    (1, 128, 16, 1, LLAMA4, 1, {}, False),                     # a single token
+    (4096, 4096, 8, 0, RENORMALIZE_NAIVE, 2, {}, False),       # mixtral_prefill's gate
+    (512, 7168, 256, 1, DEEPSEEKV3, 8, dict(n_group=8, topk_group=4, routed_scaling_factor=2.5),
+     False),                                                   # dsv3_layer's gate with FSE
+    (1000, 512, 64, 0, SIGMOID_RENORM, 4, {}, False),
+    (257, 512, 256, 0, GROUPED_TOPK, 8, dict(n_group=8, topk_group=4, routed_scaling_factor=2.5),
+     False),
+    (200, 256, 96, 0, MINIMAX2, 6, {}, False),
+    (100, 512, 33, 0, DEFAULT, 3, {}, False),
+    (100, 256, 64, 1, RENORMALIZE, 6, {}, False),
+    (300, 128, 16, 0, RENORMALIZE_NAIVE, 4, {}, True),         # integer logits: ties
+    (300, 128, 16, 0, DEEPSEEKV3, 4, dict(n_group=4, topk_group=2), True),
+    (300, 128, 32, 0, GROUPED_TOPK, 4, dict(n_group=8, topk_group=2), True),
+]
+
+
+@pytest.mark.parametrize("case", GATE_ROUTE_CASES,
+                         ids=lambda c: "T{}H{}E{}s{}m{}k{}{}".format(*c[:6], "-int" if c[7] else ""))
+def test_gate_route_fused(moe, case):
+    """The gate with routing fused into its epilogue: the logits it writes equal moe_gate's,
+    and its ids and scales equal moe_route's on those logits, bit for bit; ids bit-exact and
+    scales within 1e-6 against the oracle routing the same fp32 logits."""
+    T, H, E, ns, method, k, kw, ints = case
+    g = torch.Generator().manual_seed(T + H + E)
+    if ints:   # entries in {-1, 0, 1}: every logit an exact integer
+        x = torch.randint(-1, 2, (T, H), generator=g).to(torch.bfloat16).cuda()
+        wg = torch.randint(-1, 2, (E + ns, H), generator=g).to(torch.bfloat16).cuda()
+    else:
+        x = torch.randn(T, H, generator=g).to(torch.bfloat16).cuda()
+        wg = (torch.randn(E + ns, H, generator=g) * H ** -0.5).to(torch.bfloat16).cuda()
+    bias = (torch.randn(E, generator=g) * 0.1).cuda() if method in (DEEPSEEKV3, MINIMAX2) else None
+    lg, sg = moe.moe_gate(x, wg, E)
+    ids, sc, lg2, sg2 = moe.moe_gate_route(x, wg, method, k, E, bias=bias, want_logits=True, **kw)
+    ids3, sc3, lg3, _ = moe.moe_gate_route(x, wg, method, k, E, bias=bias, **kw)
+    torch.cuda.synchronize()
+    assert lg3 is None
+    assert torch.equal(lg2, lg)
+    if ns:
+        assert torch.equal(sg2, sg)
+    ids_r, sc_r = moe.moe_route(lg, method, k, bias=bias, **kw)
+    assert torch.equal(ids, ids_r)
+    assert torch.equal(sc.view(torch.int32), sc_r.view(torch.int32))
+    assert torch.equal(ids3, ids) and torch.equal(sc3, sc)
+    ids_ref, sc_ref = oracle.route(lg.cpu().numpy(), method, k,
+                                   bias=None if bias is None else bias.cpu().numpy(), **kw)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(sc.cpu().numpy(), sc_ref, rtol=1e-6, atol=0)
+
+
 def test_forward_with_the_fused_shared_gate(moe):
     T, H, I, E, k, sI = 300, 256, 192, 8, 2, 128
     c = _random_case(T, H, I, E, k, sI, seed=5)
