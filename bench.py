@@ -451,7 +451,7 @@ def measure(name: str, args, rank: int, world: int, dev, headline: bool) -> dict
         for _ in range(3):
             moe.moe_gate_route(x, wg, w.method, w.k, w.E, ids=ids_g, scales=sc_g,
                                shared_logits=sg_g, stream=stream, **rkw)
-        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(reps)]
         torch.cuda.synchronize()
         torch.cuda._sleep(20_000_000)
         for i in range(reps):
@@ -465,11 +465,17 @@ def measure(name: str, args, rank: int, world: int, dev, headline: bool) -> dict
             moe.moe_gate(x, wg, w.E, lg_g, sg_g, stream=stream)
             moe.moe_route(lg_g, w.method, w.k, ids=ids_s, scales=sc_s, stream=stream, **rkw)
             fev[i][3].record(stream)
+            flush(i)
+            fev[i][4].record(stream)
+            moe.moe_route(lg_g, w.method, w.k, ids=ids_s, scales=sc_s, stream=stream, **rkw)
+            fev[i][5].record(stream)
         torch.cuda.synchronize()
         gate["gate_route_fused_ms"] = round(statistics.median(
             fev[i][0].elapsed_time(fev[i][1]) for i in range(reps)), 4)
         gate["gate_then_route_ms"] = round(statistics.median(
             fev[i][2].elapsed_time(fev[i][3]) for i in range(reps)), 4)
+        gate["route_alone_ms"] = round(statistics.median(
+            fev[i][4].elapsed_time(fev[i][5]) for i in range(reps)), 4)
         gate["fused_same_ids"] = bool(torch.equal(ids_g, ids_s))
 
     # ---- end to end through the public API: every step copies its inputs (x, logits)

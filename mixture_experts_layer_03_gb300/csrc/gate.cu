@@ -39,14 +39,27 @@ constexpr int kGateRingBytes = 4 * (kGateXBytes + kGateWMaxBytes);   // 192 KB o
 constexpr int kGateSmemBytes = 1024 + kGateRingBytes;
 constexpr int kGateMaxSplit = 8;             // portable cluster size
 // Routing scratch of the fused gate + route kernel, inside the (by then idle) stage ring,
-// past the partial tile (at most 128 rows x 260 floats = 130 KB): per warp 256 keys and
-// 256 exact-key flags.
+// past the partial tile (at most 128 rows x 260 floats = 130 KB): per warp 256 keys, 256
+// exact-key flags and a 256-entry list; then the per-token slot records of up to 128 rows.
 constexpr int kGateRouteScratch = 136 * 1024;
-static_assert(kGateRouteScratch >= 128 * (256 + 4) * 4, "routing scratch overlaps the partial tile");
-static_assert(kGateRouteScratch + 4 * (256 * 4 + 256) <= kGateRingBytes, "routing scratch past the ring");
 
 // Routing done in the fused kernel's epilogue.
 enum GateRoute { kGateNoRoute = 0, kGateRoutePlain = 1, kGateRouteKeyed = 2, kGateRouteGroupedTopk = 3 };
+
+// Threads per CTA. Warps 0-3 run the GEMM (producer, MMA issuer) and read the accumulator
+// out of TMEM (warp w reaches TMEM lanes 32w..32w+31). With routing fused in, 16 warps: the
+// routing of one token is a long dependent chain (up to about 2,600 instructions for the
+// grouped methods), so the CTA's tokens (128 / cluster size of them) are spread over as
+// many warps as possible, ideally one token each.
+constexpr int gate_threads(int route) { return route == kGateNoRoute ? 128 : 512; }
+constexpr int kGateRouteWarps = 16;
+static_assert(kGateRouteScratch >= 128 * (256 + 4) * 4, "routing scratch overlaps the partial tile");
+constexpr int kGateWarpScratch = 256 * 4 + 256 + 256;            // keys, flags, list
+constexpr int kGateSlotsOff = kGateRouteScratch + kGateRouteWarps * kGateWarpScratch;
+constexpr int kGateSlots = 128 * 8;                                 // rows x kMaxTopK
+constexpr int kGateSlotBytes = kGateSlots * (4 + 4 + 8 + 4) + 128 * 8;   // sel, l, e, ek; z
+static_assert(kGateSlotsOff % 16 == 0, "slot records must stay aligned");
+static_assert(kGateSlotsOff + kGateSlotBytes <= kGateRingBytes, "routing scratch past the ring");
 static_assert(kGateBK == static_cast<int>(kMapBoxCols), "tensor-map boxes are one K block wide");
 
 struct GateArgs {
@@ -73,7 +86,7 @@ struct GateArgs {
 
 // kRoute: GateRoute; EPL: routed experts per lane of the routing warps (E <= 32 * EPL).
 template <int EPL, int kRoute>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(gate_threads(kRoute), 1)
 gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
             GateArgs g) {
   extern __shared__ uint8_t smem_raw[];
@@ -168,11 +181,13 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
   }
   __syncwarp();
 
-  // Partial tile: TMEM lane (token row) 32 * warp + lane, columns 0..n_mma-1.
-  const bool done = mbar_wait(&acc_bar, 0, abort);
-  if (!__all_sync(0xffffffffu, done)) *abort = 1;
-  tc_fence_after();
-  {
+  // Partial tile: TMEM lane (token row) 32 * warp + lane, columns 0..n_mma-1, read by
+  // warps 0-3. Warps past them (routing) go straight to the cluster barrier instead of
+  // polling the accumulator barrier beside the producer and the MMA issuer.
+  if (warp < 4) {
+    const bool done = mbar_wait(&acc_bar, 0, abort);
+    if (!__all_sync(0xffffffffu, done)) *abort = 1;
+    tc_fence_after();
     const int row = 32 * warp + lane;
     float v[16];
     for (int c0 = 0; c0 < n_mma; c0 += 16) {
@@ -230,27 +245,42 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
     }
   }
   if (kRoute != kGateNoRoute && col_tile == 0) {
-    // Route this CTA's tokens on their reduced logits (columns 0..E-1 of the rows).
+    // Route this CTA's tokens on their reduced logits (columns 0..E-1 of the rows): one warp
+    // selects each token's experts, then the block computes the weights of all the (token,
+    // slot) pairs packed across its threads.
     __syncthreads();
-    float* skey = reinterpret_cast<float*>(smem + kGateRouteScratch) + warp * 256;
-    uint8_t* sexact = smem + kGateRouteScratch + 4 * 256 * 4 + warp * 256;
-    for (int row = r0 + warp; row < r1; row += 4) {
+    const int nwarps = gate_threads(kRoute) / 32;
+    uint8_t* ws = smem + kGateRouteScratch + warp * kGateWarpScratch;
+    float* skey = reinterpret_cast<float*>(ws);
+    uint8_t* sexact = ws + 256 * 4;
+    uint8_t* slist = ws + 256 * 4 + 256;
+    uint8_t* so = smem + kGateSlotsOff;
+    const PairSlots ps{reinterpret_cast<int*>(so),
+                       reinterpret_cast<float*>(so + kGateSlots * 4),
+                       reinterpret_cast<double*>(so + kGateSlots * 8),
+                       reinterpret_cast<float*>(so + kGateSlots * 16),
+                       reinterpret_cast<double*>(so + kGateSlots * 20)};
+    for (int row = r0 + warp; row < r1; row += nwarps) {
       const int64_t t = row0 + row;
       if (t >= g.T) break;
       const float* lrow = partial + row * pstride;
+      int sel[kMaxTopK];
       if (kRoute == kGateRouteGroupedTopk) {
-        grouped_topk_token<EPL>(lrow, g.E, g.k, g.n_group, g.topk_group, g.rsf, lane, skey,
-                                g.ids + t * g.k, g.scales + t * g.k);
+        grouped_topk_select_token<EPL>(lrow, g.E, g.k, g.n_group, g.topk_group, lane, skey, sel);
       } else {
-        int sel[kMaxTopK];
         double z = 0.0;
         select_token<EPL, kRoute == kGateRouteKeyed>(lrow, g.E, g.bias, g.method, g.k, g.n_group,
-                                                     g.topk_group, lane, skey, sexact, sel, &z);
-        token_weights_warp<kRoute == kGateRouteKeyed>(lrow, sel, g.k, g.method, z, g.rsf, lane,
-                                                      g.ids + t * g.k, g.scales + t * g.k);
+                                                     g.topk_group, lane, skey, sexact, slist, sel,
+                                                     &z);
+        if (kRoute == kGateRoutePlain && g.method == MOE_ROUTE_DEFAULT && lane == 0)
+          ps.z[row - r0] = z;
       }
+      record_selection(lrow, sel, g.k, lane, ps, row - r0);
       __syncwarp();
     }
+    __syncthreads();
+    block_pair_weights<kRoute == kGateRouteGroupedTopk ? 2 : kRoute == kGateRouteKeyed ? 1 : 0>(
+        r1 - r0, row0 + r0, g.T, g.k, g.method, g.rsf, ps, g.ids, g.scales);
   }
   cluster_sync();   // no CTA leaves while another reads its shared memory
   if (tid == 0 && *abort && g.status) atomicOr(g.status, MOE_DEVICE_FLAG_TIMEOUT);
@@ -277,10 +307,12 @@ cudaError_t gate_smem_optin() {
 }
 
 template <int EPL, int kRoute>
-cudaError_t launch_gate_t(const cudaLaunchConfig_t& cfg, const CUtensorMap& mx,
+cudaError_t launch_gate_t(const cudaLaunchConfig_t& cfg0, const CUtensorMap& mx,
                           const CUtensorMap& mw, const GateArgs& g) {
   const cudaError_t e = gate_smem_optin<EPL, kRoute>();
   if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = cfg0;
+  cfg.blockDim = dim3(gate_threads(kRoute));
   return cudaLaunchKernelEx(&cfg, gate_kernel<EPL, kRoute>, mx, mw, g);
 }
 
@@ -356,7 +388,6 @@ moe_status launch_gate(const void* x, const void* wg, int64_t T, int H, int E, i
     return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (gate)");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * S));
-  cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = kGateSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];

@@ -61,87 +61,59 @@ route_kernel(const float* __restrict__ logits, int64_t T, int E, const float* __
              int32_t* __restrict__ ids, float* __restrict__ scales) {
   __shared__ float s_key[kRouteWarps][256];
   __shared__ uint8_t s_exact[kRouteWarps][256];
-  __shared__ float s_sel_l[kRouteWarps][kMaxTopK];
-  __shared__ double s_e[kRouteWarps][kMaxTopK];
+  __shared__ uint8_t s_list[kRouteWarps][256];
+  __shared__ int s_sel[kRouteWarps * kMaxTopK];
+  __shared__ float s_sel_l[kRouteWarps * kMaxTopK];
+  __shared__ double s_e[kRouteWarps * kMaxTopK];
   __shared__ double s_z[kRouteWarps];
+  const PairSlots ps{s_sel, s_sel_l, s_e, nullptr, s_z};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp;
-  const bool valid = t < T;   // warp-uniform; invalid warps still reach the block barriers
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRouteWarps;
+  const int64_t t = t0 + warp;
   pdl_trigger();
   pdl_wait();
 
-  if (valid) {
+  if (t < T) {   // warp-uniform; every warp reaches the block barriers below
     const float* row = logits + t * E;
     int sel[kMaxTopK];
     double z = 0.0;
-    select_token<EPL, kGrouped>(row, E, bias, method, k, n_group, topk_group, lane,
-                                s_key[warp], s_exact[warp], sel, &z);
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      if (j < k && lane == j) {
-        ids[t * k + j] = sel[j];
-        const float v = row[sel[j]];
-        s_sel_l[warp][j] = isfinite(v) ? v : -INFINITY;
-      }
-    }
+    select_token<EPL, kGrouped>(row, E, bias, method, k, n_group, topk_group, lane, s_key[warp],
+                                s_exact[warp], s_list[warp], sel, &z);
+    record_selection(row, sel, k, lane, ps, warp);
     if (!kGrouped && method == MOE_ROUTE_DEFAULT && lane == 0) s_z[warp] = z;
   }
   __syncthreads();
-
-  // Weights of the block's (token, slot) pairs, packed across threads.
-  const int npairs = kRouteWarps * k;
-  for (int pidx = threadIdx.x; pidx < npairs; pidx += blockDim.x) {
-    const int w = pidx / k, j = pidx - w * k;
-    const int64_t tt = static_cast<int64_t>(blockIdx.x) * kRouteWarps + w;
-    if (tt >= T) continue;
-    const double lv = static_cast<double>(s_sel_l[w][j]);
-    double e;
-    if (kGrouped || method == MOE_ROUTE_SIGMOID_RENORM || method == MOE_ROUTE_LLAMA4)
-      e = sigmoid_d(lv);
-    else
-      e = exp(lv - static_cast<double>(s_sel_l[w][0]));   // slot 0 holds the largest logit
-    s_e[w][j] = e;
-  }
-  __syncthreads();
-  for (int pidx = threadIdx.x; pidx < npairs; pidx += blockDim.x) {
-    const int w = pidx / k, j = pidx - w * k;
-    const int64_t tt = static_cast<int64_t>(blockIdx.x) * kRouteWarps + w;
-    if (tt >= T) continue;
-    double s = 0.0;
-    for (int q = 0; q < k; ++q) s += s_e[w][q];
-    double wgt;
-    if (method == MOE_ROUTE_DEFAULT)
-      wgt = s_e[w][j] / s_z[w];
-    else if (method == MOE_ROUTE_LLAMA4)
-      wgt = s_e[w][j];
-    else if (method == MOE_ROUTE_MINIMAX2)
-      wgt = s_e[w][j] / s;
-    else if (kGrouped)
-      wgt = s_e[w][j] / (s + 1e-20) * static_cast<double>(rsf);
-    else
-      wgt = s_e[w][j] / s;
-    scales[tt * k + j] = __double2float_rn(wgt);
-  }
+  block_pair_weights<kGrouped ? 1 : 0>(kRouteWarps, t0, T, k, method, rsf, ps, ids, scales);
 }
 
-
+// vLLM grouped top-k: the same block structure, selection by grouped_topk_select_token.
 template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_grouped_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int n_group,
                           int topk_group, float rsf, int32_t* __restrict__ ids,
                           float* __restrict__ scales) {
   __shared__ float s_key[kRouteWarps][256];
+  __shared__ int s_sel[kRouteWarps * kMaxTopK];
+  __shared__ float s_sel_l[kRouteWarps * kMaxTopK];
+  __shared__ double s_e[kRouteWarps * kMaxTopK];
+  __shared__ float s_ek[kRouteWarps * kMaxTopK];
+  const PairSlots ps{s_sel, s_sel_l, s_e, s_ek, nullptr};
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteWarps + warp;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRouteWarps;
+  const int64_t t = t0 + warp;
   pdl_trigger();
   pdl_wait();
-  if (t >= T) return;   // warp-uniform; the kernel has no block-wide barrier
-
-  grouped_topk_token<EPL>(logits + t * E, E, k, n_group, topk_group, rsf, lane, s_key[warp],
-                          ids + t * k, scales + t * k);
+  if (t < T) {
+    const float* row = logits + t * E;
+    int sel[kMaxTopK];
+    grouped_topk_select_token<EPL>(row, E, k, n_group, topk_group, lane, s_key[warp], sel);
+    record_selection(row, sel, k, lane, ps, warp);
+  }
+  __syncthreads();
+  block_pair_weights<2>(kRouteWarps, t0, T, k, MOE_ROUTE_GROUPED_TOPK, rsf, ps, ids, scales);
 }
 
 template <int EPL>

@@ -119,6 +119,31 @@ __device__ __forceinline__ bool warp_topk_separated(const float (&key)[EPL], uin
   return sep;
 }
 
+// Replaces the approximate keys of the experts marked 2 in s_exact by their exact keys
+// fl32(fl32(sigmoid_fp64(l)) + b) and marks them 1. The marked experts are first listed in
+// s_list (expert ids, 256 bytes per warp), then each lane takes every 32nd entry.
+template <int EPL>
+__device__ __forceinline__ void make_marked_exact(const float* row, const float* bias, int E,
+                                                  int lane, float* s_key, uint8_t* s_exact,
+                                                  uint8_t* s_list) {
+  int n = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    const bool m = e < E && s_exact[e] == 2;
+    const uint32_t b = __ballot_sync(0xffffffffu, m);
+    if (m) s_list[n + __popc(b & ((1u << lane) - 1u))] = static_cast<uint8_t>(e);
+    n += __popc(b);
+  }
+  __syncwarp();
+  for (int j = lane; j < n; j += 32) {
+    const int e = s_list[j];
+    s_key[e] = exact_kappa(row[e], bias ? bias[e] : 0.0f);
+    s_exact[e] = 1;
+  }
+  __syncwarp();
+}
+
 // Selection of one token's k experts by one warp: `row` holds the token's E fp32 logits
 // (global or shared memory); s_key / s_exact are this warp's scratch (256 floats and 256
 // bytes of shared memory). On return sel[0..k) holds the chosen experts by descending key
@@ -130,7 +155,8 @@ template <int EPL, bool kGrouped>
 __device__ __forceinline__ void select_token(const float* row, int E, const float* bias,
                                              int method, int k, int n_group, int topk_group,
                                              int lane, float* s_key, uint8_t* s_exact,
-                                             int (&sel)[kMaxTopK], double* z_out) {
+                                             uint8_t* s_list, int (&sel)[kMaxTopK],
+                                             double* z_out) {
   float l[EPL], key[EPL];
   uint32_t present = 0;
 #pragma unroll
@@ -218,12 +244,12 @@ __device__ __forceinline__ void select_token(const float* row, int E, const floa
     }
 
     if (!certain) {
-      // Exact path (rare): exact keys wherever a decision could depend on them.
-      // Group scores: lane g sums the exact top-2 keys of its group. Only experts whose
-      // approximate key is within 2D of the approximate second-largest can be in the
-      // exact top-2; their keys are made exact first.
-      float gscore = -INFINITY;
-      int gidx = INT32_MAX;
+      // Exact path (rare): exact keys wherever a decision could depend on them, computed
+      // one per lane over a list of the experts concerned (marked 2 in s_exact), so that
+      // the fp64 sigmoids of a token run side by side rather than lane after lane.
+      // Group scores: only experts whose approximate key is within 2D of their group's
+      // approximate second largest can be in its exact top-2 (every other expert's exact
+      // key lies below the exact second largest), so those are made exact first.
       if (n_group > 1 && lane < n_group) {
         const int e0 = lane * epg;
         float a1 = -INFINITY, a2 = -INFINITY;
@@ -232,18 +258,19 @@ __device__ __forceinline__ void select_token(const float* row, int E, const floa
           if (v > a1) { a2 = a1; a1 = v; } else if (v > a2) { a2 = v; }
         }
         const float thr = a2 - 2.0f * D;
+        for (int j = 0; j < epg; ++j)
+          if (s_key[e0 + j] >= thr && !s_exact[e0 + j]) s_exact[e0 + j] = 2;
+      }
+      __syncwarp();
+      make_marked_exact<EPL>(row, bias, E, lane, s_key, s_exact, s_list);
+      float gscore = -INFINITY;
+      int gidx = INT32_MAX;
+      if (n_group > 1 && lane < n_group) {
+        const int e0 = lane * epg;
         float x1 = -INFINITY, x2 = -INFINITY;
         for (int j = 0; j < epg; ++j) {
-          const int e = e0 + j;
-          float v = s_key[e];
-          if (v >= thr) {
-            if (!s_exact[e]) {
-              v = exact_kappa(row[e], bias ? bias[e] : 0.0f);
-              s_key[e] = v;
-              s_exact[e] = 1;
-            }
-            if (v > x1) { x2 = x1; x1 = v; } else if (v > x2) { x2 = v; }
-          }
+          const float v = s_key[e0 + j];
+          if (v > x1) { x2 = x1; x1 = v; } else if (v > x2) { x2 = v; }
         }
         gscore = __fadd_rn(x1, x2);
         gidx = lane;
@@ -258,7 +285,6 @@ __device__ __forceinline__ void select_token(const float* row, int E, const floa
         if (v.idx == lane) gtaken = true;
         chosen |= 1u << v.idx;
       }
-      __syncwarp();
 
       // Final top-k inside the chosen groups. Bounds per expert (exact: lb = ub = kappa);
       // the k-th largest lower bound is a threshold no non-candidate can reach.
@@ -286,10 +312,15 @@ __device__ __forceinline__ void select_token(const float* row, int E, const floa
           const float ub = ex ? key[i] : key[i] + D;
           if (ub >= kth_lb) {
             cand |= 1u << i;
-            if (!ex) key[i] = exact_kappa(row[e], bias ? bias[e] : 0.0f);
+            if (!ex) s_exact[e] = 2;
           }
         }
       }
+      __syncwarp();
+      make_marked_exact<EPL>(row, bias, E, lane, s_key, s_exact, s_list);
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if ((cand >> i) & 1u) key[i] = s_key[lane + 32 * i];
       warp_topk(key, cand, k, lane, sel, nullptr);
     }
   } else {
@@ -400,12 +431,12 @@ __device__ __forceinline__ bool grouped_topk_select(const float (&key)[EPL], con
 
 // vLLM grouped top-k (sigmoid scoring) of one token by one warp: `row` holds its E fp32
 // logits (global or shared memory), s_key is this warp's scratch (256 floats of shared
-// memory); writes the token's k ids and weights (ids_row, scales_row: its k slots).
+// memory). On return sel[0..k) holds the chosen experts (uniform across the warp), group
+// by group; block_pair_weights orders them by key and weights them.
 template <int EPL>
-__device__ __forceinline__ void grouped_topk_token(const float* row, int E, int k, int n_group,
-                                                   int topk_group, float rsf, int lane,
-                                                   float* s_key, int32_t* ids_row,
-                                                   float* scales_row) {
+__device__ __forceinline__ void grouped_topk_select_token(const float* row, int E, int k,
+                                                          int n_group, int topk_group, int lane,
+                                                          float* s_key, int (&sel)[kMaxTopK]) {
   float l[EPL], key[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
@@ -425,9 +456,10 @@ __device__ __forceinline__ void grouped_topk_token(const float* row, int E, int 
   // exact key adds one rounding: 1.25e-6 bounds the difference with a wide margin.
   constexpr float D = 1.25e-6f;
   const int per = k / topk_group;
-  int sel[kMaxTopK];
-  bool certain = grouped_topk_select(key, s_key, E, n_group, topk_group, per, lane, true, D, sel);
+  const bool certain = grouped_topk_select(key, s_key, E, n_group, topk_group, per, lane, true, D,
+                                           sel);
   if (!certain) {
+    // Every key exact (fp64 sigmoid rounded once), EPL per lane side by side.
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
@@ -439,77 +471,91 @@ __device__ __forceinline__ void grouped_topk_token(const float* row, int E, int 
     __syncwarp();
     grouped_topk_select(key, s_key, E, n_group, topk_group, per, lane, false, 0.0f, sel);
   }
+}
 
-  // Lane j < k: the j-th chosen expert's exact score and key; its slot is the number of
-  // chosen experts that beat it (larger key, or the same key and a lower index).
-  int me = INT32_MAX;
+// Per-token routing record of a block, kept in shared memory between the selection (one
+// warp per token) and block_pair_weights: slot j of token r is entry r * kMaxTopK + j.
+struct PairSlots {
+  int* sel;        // chosen expert
+  float* sel_l;    // its logit (non-finite as -inf)
+  double* e;       // its fp64 score
+  float* ek;       // its exact fp32 key (grouped top-k ordering)
+  double* z;       // [rows] Default: softmax normaliser over all E
+};
+
+// Lane j < k of the warp that selected token r records slot j.
+__device__ __forceinline__ void record_selection(const float* row, const int (&sel)[kMaxTopK],
+                                                 int k, int lane, const PairSlots& ps, int r) {
 #pragma unroll
-  for (int q = 0; q < kMaxTopK; ++q)
-    if (q < k && q == lane) me = sel[q];
-  double s = 0.0;
-  float ek = -INFINITY;
-  if (lane < k) {
-    const float v = row[me];
-    s = isfinite(v) ? sigmoid_d(static_cast<double>(v)) : 0.0;   // non-finite counts as -inf
-    ek = __double2float_rn(s);
-  }
-  int slot = 0;
-  for (int q = 0; q < k; ++q) {
-    const float ok = __shfl_sync(0xffffffffu, ek, q);
-    const int oe = __shfl_sync(0xffffffffu, me, q);
-    if (q != lane && beats(ok, oe, ek, me)) ++slot;
-  }
-  const double sum = warp_sum_d(s);
-  if (lane < k) {
-    ids_row[slot] = me;
-    scales_row[slot] = __double2float_rn(s / sum * static_cast<double>(rsf));
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j < k && lane == j) {
+      const float v = row[sel[j]];
+      ps.sel[r * kMaxTopK + j] = sel[j];
+      ps.sel_l[r * kMaxTopK + j] = isfinite(v) ? v : -INFINITY;
+    }
   }
 }
 
-
-// Weights of one token's k chosen experts (sel, from select_token), one per lane j < k,
-// written with the ids to the token's slots. The same arithmetic as the route kernel's
-// packed weights: fp64 sigmoid (sigmoid methods) or exp(l - l_max) (softmax methods) of
-// the chosen logits, their sum taken in slot order, one rounding to fp32.
-template <bool kGrouped>
-__device__ __forceinline__ void token_weights_warp(const float* row, const int (&sel)[kMaxTopK],
-                                                   int k, int method, double z, float rsf,
-                                                   int lane, int32_t* ids_row,
-                                                   float* scales_row) {
-  int me = 0;
-#pragma unroll
-  for (int q = 0; q < kMaxTopK; ++q)
-    if (q < k && q == lane) me = sel[q];
-  float lv = -INFINITY;
-  if (lane < k) {
-    const float v = row[me];
-    lv = isfinite(v) ? v : -INFINITY;
-  }
-  const double l0 = static_cast<double>(__shfl_sync(0xffffffffu, lv, 0));   // the largest
-  double e = 0.0;
-  if (lane < k) {
-    if (kGrouped || method == MOE_ROUTE_SIGMOID_RENORM || method == MOE_ROUTE_LLAMA4)
-      e = sigmoid_d(static_cast<double>(lv));
+// Weights of the block's nrows tokens (t0 + r, r < nrows; tokens at or past T skipped),
+// their (token, slot) pairs packed across the block's threads: FP64 runs at 1/64 of the
+// FP32 rate on this part, so a warp that held one token's k pairs would issue mostly idle
+// fp64 instructions. Scores: fp64 sigmoid of the chosen logit (sigmoid methods, keyed and
+// grouped top-k) or exp(l - l_max) (softmax methods; slot 0 holds the largest logit); their
+// sum taken in slot order; one rounding to fp32. kMode: 0 logit-keyed methods, 1 biased
+// sigmoid keys (DeepSeekV3, MiniMax2), 2 vLLM grouped top-k (slots ordered here by the
+// exact key, ties to the lower expert index). Called by every thread of the block; it
+// synchronises the block twice.
+template <int kMode>
+__device__ __forceinline__ void block_pair_weights(int nrows, int64_t t0, int64_t T, int k,
+                                                   int method, float rsf, const PairSlots& ps,
+                                                   int32_t* ids, float* scales) {
+  const int npairs = nrows * k;
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
+    const int r = p / k, j = p - r * k;
+    if (t0 + r >= T) continue;
+    const double lv = static_cast<double>(ps.sel_l[r * kMaxTopK + j]);
+    double e;
+    if (kMode != 0 || method == MOE_ROUTE_SIGMOID_RENORM || method == MOE_ROUTE_LLAMA4)
+      e = sigmoid_d(lv);
     else
-      e = exp(static_cast<double>(lv) - l0);
+      e = exp(lv - static_cast<double>(ps.sel_l[r * kMaxTopK]));
+    ps.e[r * kMaxTopK + j] = e;
+    if (kMode == 2) ps.ek[r * kMaxTopK + j] = __double2float_rn(e);
   }
-  double s = 0.0;
-  for (int q = 0; q < k; ++q) s += __shfl_sync(0xffffffffu, e, q);
-  if (lane < k) {
+  __syncthreads();
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
+    const int r = p / k, j = p - r * k;
+    const int64_t t = t0 + r;
+    if (t >= T) continue;
+    const double* er = ps.e + r * kMaxTopK;
+    double s = 0.0;
+    for (int q = 0; q < k; ++q) s += er[q];
     double wgt;
-    if (method == MOE_ROUTE_DEFAULT)
-      wgt = e / z;
+    if (kMode == 2)
+      wgt = er[j] / s * static_cast<double>(rsf);
+    else if (method == MOE_ROUTE_DEFAULT)
+      wgt = er[j] / ps.z[r];
     else if (method == MOE_ROUTE_LLAMA4)
-      wgt = e;
+      wgt = er[j];
     else if (method == MOE_ROUTE_MINIMAX2)
-      wgt = e / s;
-    else if (kGrouped)
-      wgt = e / (s + 1e-20) * static_cast<double>(rsf);
+      wgt = er[j] / s;
+    else if (kMode == 1)
+      wgt = er[j] / (s + 1e-20) * static_cast<double>(rsf);
     else
-      wgt = e / s;
-    ids_row[lane] = me;
-    scales_row[lane] = __double2float_rn(wgt);
+      wgt = er[j] / s;
+    const int me = ps.sel[r * kMaxTopK + j];
+    int slot = j;
+    if (kMode == 2) {
+      const float* ekr = ps.ek + r * kMaxTopK;
+      const int* sr = ps.sel + r * kMaxTopK;
+      slot = 0;
+      for (int q = 0; q < k; ++q)
+        if (q != j && beats(ekr[q], sr[q], ekr[j], me)) ++slot;
+    }
+    ids[t * k + slot] = me;
+    scales[t * k + slot] = __double2float_rn(wgt);
   }
+  __syncthreads();
 }
 
 }  // namespace
