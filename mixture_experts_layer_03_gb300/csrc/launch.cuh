@@ -3,11 +3,14 @@
 // Every kernel of the library is launched with programmatic stream serialization
 // allowed. Each kernel calls pdl_trigger() at entry, so the next kernel on the stream
 // may be scheduled as soon as all of this kernel's CTAs are resident, and calls
-// pdl_wait() before its first access to global memory, which returns only once the
-// previous kernel on the stream has completed and its writes are visible. Only work
-// that touches no global memory (shared-memory setup, TMEM allocation, tensor-map
-// prefetch) overlaps the previous kernel, so stream order is preserved by construction.
-// Without a preceding kernel both calls are no-ops.
+// pdl_wait() before its first access to global memory that a previous kernel may write
+// or that a previous kernel may still read, which returns only once the previous kernel
+// on the stream has completed and its writes are visible. Before that wait a kernel does
+// only work that neither reads what an earlier kernel writes nor writes anything:
+// shared-memory setup, TMEM allocation, tensor-map prefetch, and (the narrow grouped-GEMM
+// launch) L2 prefetches of expert weight tiles, which are inputs of the whole forward
+// that no kernel of the library writes. Stream order is therefore preserved by
+// construction. Without a preceding kernel both calls are no-ops.
 #pragma once
 
 #include <utility>
