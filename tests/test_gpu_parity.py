@@ -260,10 +260,13 @@ SMALL_CASES = [
     (150, 256, 192, 4, 1, 0, "one_expert"),    # single-SM: 1 full tile + 22 rows (16-row X boxes)
     (180, 256, 192, 4, 1, 0, "one_expert"),    # single-SM: 1 full tile + 52 rows (64-row X box)
     (2200, 256, 192, 4, 2, 256, "route"),      # CTA pairs for routed and shared groups
-    # CTA-pair weight-major leftover units of 1, 16 and 128 rows beside full units
+    # CTA-pair weight-major leftover units of 1, 16, 32, 33 and 128 rows beside full units
     (640, 512, 320, 2, 2, 0, "one_expert"),    # 2 full units + 128 rows, ragged FC1 tile
+    (528, 512, 320, 2, 2, 0, "one_expert"),    # 2 full units + 16 rows, ragged FC1 tile
     (272, 256, 192, 1, 1, 0, "one_expert"),    # 1 full unit + 16 rows
     (513, 256, 192, 1, 1, 0, "one_expert"),    # 2 full units + 1 row
+    (288, 256, 192, 1, 1, 0, "one_expert"),    # 1 full unit + 32 rows
+    (289, 256, 192, 1, 1, 0, "one_expert"),    # 1 full unit + 33 rows
     (2100, 256, 192, 4, 2, 256, "route"),      # routed groups of ~1050 rows, shared 8 full + 52
     (513, 128, 128, 8, 8, 0, "route"),         # k = E: every expert every token
     (200, 192, 128, 16, 4, 128, "random_dup"), # repeated ids in a row, shared expert
