@@ -12,6 +12,9 @@
 //                  starts, offsets and the FC1/FC2 tile lists.
 //   gather_kernel  x_perm[r] = x[perm_src[r] / k] (and x[t] for the shared rows),
 //                  16-byte vector copies, one warp per row (decode-sized batches).
+//   plan_gather_kernel  plan and row copy in one launch when the problem is one chunk
+//                  and copied row by row: every block plans (block 0 publishes the plan)
+//                  and copies its rows from its own shared-memory perm_src.
 //   scatter_kernel the same rows, token-major: one warp per token reads x[t] once and
 //                  writes it to each of its permuted rows perm_inv[t*k + j] (and the
 //                  shared row). With many tokens, x is then read from HBM once instead
@@ -108,24 +111,25 @@ struct PlanArgs {
   int32_t* sched;      // [kSchedCounters + G] grouped-GEMM counters, zeroed here every forward
 };
 
-// kSingleChunk: the whole problem is one chunk (one block); the block counts its own
-// histogram and clears the status word, and no hist_kernel runs before it.
+// The plan of chunk b, by one block of kPermThreads threads. kSingleChunk: the whole
+// problem is one chunk; the block counts its own histogram (no hist_kernel ran before it).
+// publish: write the plan to the workspace (counts, starts, offsets, tile lists, perm_src,
+// perm_inv; clear the status word, flag invalid ids, zero the GEMM counters). s_src (or
+// NULL): also receives perm_src in shared memory. Returns the number of valid rows P'.
 template <bool kSingleChunk>
-__global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
+__device__ __forceinline__ int plan_body(const PlanArgs& a, int b, bool publish,
+                                         int32_t* s_src) {
   __shared__ int32_t s_run[256];                // next free row per expert in this chunk
   __shared__ int32_t s_wcnt[kPermWarps][256];   // rows per (warp, expert) in a sub-chunk
   __shared__ int s_warp[kPermWarps + 1];
   const int tid = threadIdx.x;
-  const int b = blockIdx.x;
   const int E = a.E;
-  pdl_trigger();
-  pdl_wait();
 
   // Column sums and this chunk's prefix over earlier chunks.
   int tot = 0, before = 0;
   if (kSingleChunk) {
     for (int e = tid; e < 256; e += blockDim.x) s_run[e] = 0;
-    if (tid < 4) a.status[tid] = 0;
+    if (publish && tid < 4) a.status[tid] = 0;
     __syncthreads();
     for (int64_t f = tid; f < a.P; f += blockDim.x) {
       const int e = a.ids[f];
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
   if (tid < E) s_run[tid] = off + before;
   for (int i = tid; i < kPermWarps * 256; i += blockDim.x) (&s_wcnt[0][0])[i] = 0;
 
-  if (b == 0) {
+  if (b == 0 && publish) {
     // Group table: routed experts 0..E-1, then the shared expert (all T tokens, rows
     // starting at P). Tiles per group: full 128-row tiles plus one remainder tile, times
     // the output-channel tiles of the GEMM.
@@ -217,11 +221,13 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
     if (f < f1) {
       e = a.ids[f];
       if (e < 0 || e >= E) {
-        a.perm_inv[f] = -1;
-        atomicOr(a.status, MOE_DEVICE_FLAG_BAD_ID);
+        if (publish) {
+          a.perm_inv[f] = -1;
+          atomicOr(a.status, MOE_DEVICE_FLAG_BAD_ID);
+        }
         e = -1;
       } else if (e < a.e_lo || e >= a.e_hi) {
-        a.perm_inv[f] = -1;   // another call's expert: this slot adds exactly 0 here
+        if (publish) a.perm_inv[f] = -1;   // another call's expert: this slot adds 0 here
         e = -1;
       }
     }
@@ -233,8 +239,11 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
     if (e >= 0) {
       int pos = s_run[e] + rank_in_warp;
       for (int w = 0; w < warp; ++w) pos += s_wcnt[w][e];
-      a.perm_src[pos] = static_cast<int32_t>(f);
-      a.perm_inv[f] = pos;
+      if (publish) {
+        a.perm_src[pos] = static_cast<int32_t>(f);
+        a.perm_inv[f] = pos;
+      }
+      if (s_src) s_src[pos] = static_cast<int32_t>(f);
     }
     __syncthreads();
     if (tid < E) {
@@ -246,6 +255,52 @@ __global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
       s_run[tid] += add;
     }
     __syncthreads();
+  }
+  return p_valid;
+}
+
+template <bool kSingleChunk>
+__global__ void __launch_bounds__(kPermThreads) plan_kernel(PlanArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  plan_body<kSingleChunk>(a, blockIdx.x, true, nullptr);
+}
+
+// Plan and row copy in one launch, for a problem of one chunk copied row by row (decode
+// batches): every block computes the (small) plan itself, block 0 also publishes it, and
+// each block then copies its rows, x_perm[r] = x[perm_src[r] / k] (and x[t] for the shared
+// rows), from its own copy of perm_src. One kernel boundary fewer on the way to the GEMM.
+__global__ void __launch_bounds__(kPermThreads)
+plan_gather_kernel(PlanArgs a, const __nv_bfloat16* __restrict__ x, int64_t rows, int H,
+                   __nv_bfloat16* __restrict__ x_perm) {
+  __shared__ int32_t s_src[kPermChunk];
+  pdl_trigger();
+  pdl_wait();
+  const int p_valid = plan_body<true>(a, 0, blockIdx.x == 0, s_src);
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int nvec = H / 8;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       r < rows; r += warps) {
+    int64_t src;
+    if (r < a.P) {
+      if (r >= p_valid) continue;
+      src = s_src[r] / a.k;
+    } else {
+      src = r - a.P;
+    }
+    const uint4* sp = reinterpret_cast<const uint4*>(x + src * H);
+    uint4* d = reinterpret_cast<uint4*>(x_perm + r * H);
+    int v = lane;
+    for (; v + 224 < nvec; v += 256) {
+      uint4 q8[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) q8[q] = __ldg(sp + v + 32 * q);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) __stcs(d + v + 32 * q, q8[q]);
+    }
+    for (; v < nvec; v += 32) d[v] = __ldg(sp + v);
   }
 }
 
@@ -368,6 +423,19 @@ moe_status launch_permute(const moe_problem& p, const moe_ws_layout& L, const vo
   a.status = reinterpret_cast<int32_t*>(ws + L.status);
   a.sched = reinterpret_cast<int32_t*>(ws + L.sched);
   cudaError_t err;
+  if (nb == 1 && p.T < kScatterMinTokens) {
+    // One chunk, row-by-row copy: plan and copy in one launch (16 warps of rows per block).
+    const int64_t rows = L.rows;
+    int64_t blocks = (rows + kPermWarps - 1) / kPermWarps;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 4;
+    if (blocks > cap) blocks = cap;
+    err = launch_pdl(plan_gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kPermThreads),
+                     0, s, a, static_cast<const __nv_bfloat16*>(x), rows, p.H,
+                     reinterpret_cast<__nv_bfloat16*>(ws + L.x_perm));
+    if (err != cudaSuccess)
+      return set_error(MOE_ERR_CUDA, "permute launch: %s", cudaGetErrorString(err));
+    return MOE_OK;
+  }
   if (nb == 1) {
     err = launch_pdl(plan_kernel<true>, dim3(1), dim3(kPermThreads), 0, s, a);
   } else {
