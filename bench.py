@@ -329,10 +329,12 @@ def measure(name: str, args, rank: int, world: int, dev, headline: bool) -> dict
         moe.moe_route(lg, w.method, w.k, stream=s, **route_kw)
         moe.moe_forward(xx, ids, sc, w13, w2, w13s, w2s, y=y, workspace=ws, stream=s)
 
-    # route; permute (the histogram kernel only with more than one 1024-pair chunk, the
-    # plan kernel, the row copy); FC1 and FC2 in one persistent GEMM launch (CTA-pair
+    # route; permute (with more than one 1024-pair chunk: the histogram kernel, the plan
+    # kernel and the row copy; with one chunk copied row by row, i.e. below 2048 tokens:
+    # plan and copy in one kernel); FC1 and FC2 in one persistent GEMM launch (CTA-pair
     # kernel when T*k >= 256*E, else single-SM); finalize
-    launches_per_step = 1 + (3 if ws.layout["n_chunks"] > 1 else 2) + 1 + 1
+    n_permute = 3 if ws.layout["n_chunks"] > 1 else (1 if w.T < 2048 else 2)
+    launches_per_step = 1 + n_permute + 1 + 1
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
