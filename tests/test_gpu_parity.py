@@ -133,6 +133,21 @@ def test_route_nonfinite_logits_never_beat_finite(moe):
     assert not np.isin(ids.cpu().numpy(), [3, 5, 7]).any()
 
 
+def test_grouped_topk_nonfinite_logits(moe):
+    """Non-finite logits count as -inf (score 0) in the grouped top-k as well: they lower
+    their group's total and are chosen only when a kept group has nothing better."""
+    g = torch.Generator().manual_seed(31)
+    logits = torch.randn(40, 32, generator=g)
+    logits[:, 1] = float("nan")
+    logits[:, 9] = float("inf")
+    logits[:, 17] = -float("inf")
+    logits[5, 24:28] = -float("inf")       # a whole group without a finite logit
+    ids, sc = moe.moe_route(logits.cuda(), GROUPED_TOPK, 4, n_group=8, topk_group=2)
+    ids_ref, sc_ref = oracle.route(logits.numpy(), GROUPED_TOPK, 4, n_group=8, topk_group=2)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(sc.cpu().numpy(), sc_ref, rtol=1e-6, atol=0)
+
+
 # ------------------------------------------------------------------------ permute
 
 @pytest.mark.parametrize("T,E,k", [(300, 8, 2), (5000, 64, 4), (1, 4, 1), (2048, 256, 8), (513, 16, 2),
