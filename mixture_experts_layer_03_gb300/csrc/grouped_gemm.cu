@@ -60,7 +60,14 @@ static_assert(kBK == static_cast<int>(kMapBoxCols), "tensor-map boxes are one K 
 constexpr int kRowBytes = kBK * 2;                   // one K row of a tile = the swizzle width
 constexpr int kXStageBytes = 128 * kRowBytes;        // 128 rows of X
 constexpr int kWStageBytes = 128 * kRowBytes;        // 128 rows of W
-constexpr int kStages = 6;                           // pair kernel: X + W halves, 32 KB
+// Pair kernel: six 16 KB slots each of X and W rows, one K block per slot; a pipeline
+// stage is two consecutive slots (two K blocks), so the MMA thread waits and commits once
+// per eight MMAs. That thread's own instruction latency bounds the pair kernel: at one K
+// block per stage (a try_wait, four MMAs and a commit, about 600 cycles) it issued more
+// slowly than the tensor pipe ran the four 256 x 256 x 16 MMAs.
+constexpr int kPairSlots = 6;
+constexpr int kPairBlocksPerStage = 2;
+constexpr int kStages = kPairSlots / kPairBlocksPerStage;
 constexpr int kSingleStages = 4;                     // single kernel: X + 2 W halves, 48 KB
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 512;
@@ -77,7 +84,7 @@ constexpr int kClaimLead = 4;
 constexpr int kStoreBufBytes = static_cast<int>(kStoreBoxRows * kStoreBoxCols * 2);
 constexpr int kStageAreaBytes = 4 * 2 * kStoreBufBytes;
 constexpr int kSmemBytes =
-    1024 /*alignment slack*/ + kStages * (kXStageBytes + kWStageBytes) + kStageAreaBytes;
+    1024 /*alignment slack*/ + kPairSlots * (kXStageBytes + kWStageBytes) + kStageAreaBytes;
 constexpr int kSingleSmemBytes =
     1024 + kSingleStages * (kXStageBytes + 2 * kWStageBytes) + kStageAreaBytes;
 constexpr uint16_t kPairMask = 0x3;
@@ -408,30 +415,40 @@ __device__ __forceinline__ void finish_claims(const GemmArgs& a) {
 
 // ============================================================== single-SM kernel
 
+// Shared-memory descriptor of the tile `off` bytes past the one `desc` describes. The
+// start-address field holds bits 4-17 of the shared address, and every operand here lies
+// inside the CTA's shared memory (below 228 KB), so adding off / 16 to the base
+// descriptor gives what sdesc_k_major would build from the shifted address. The MMA
+// issuer's loops are bound by its own instruction latency (a try_wait, four to eight
+// MMAs, a commit per stage), so they build no descriptor and divide nothing inside.
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t desc, uint32_t off) {
+  return desc + (off >> 4);
+}
+
 // The K loop of one tile of the single-SM kernel. Token-major: A = 128 X rows, B = the
 // 256 W rows of the stage (N = 256). Weight-major: two MMAs, A = each 128-row half of the
 // W stage, B = the tile's X rows (N = ntok), into accumulator columns 0 and 128. One loop
-// per form, as in the pair kernel. Returns false if a stage did not arrive in time.
+// per form, as in the pair kernel. dx0 / dw0 describe stage 0's X and W tiles. Returns
+// false if a stage did not arrive in time.
 template <bool kTokenMajor>
 __device__ __forceinline__ bool single_k_loop(uint32_t d, uint32_t idesc, int nkb, int& stage,
-                                              uint32_t& phase, uint32_t sx0, uint32_t sw0,
+                                              uint32_t& phase, uint64_t dx0, uint64_t dw0,
                                               uint64_t* full_bar, uint64_t* empty_bar,
                                               volatile int* abort) {
   for (int kb = 0; kb < nkb; ++kb) {
     if (!mbar_wait(&full_bar[stage], phase, abort)) return false;
     tc_fence_after();
-    const uint32_t xa = sx0 + stage * kXStageBytes;
-    const uint32_t wa = sw0 + stage * (2 * kWStageBytes);
+    const uint64_t xs = sdesc_at(dx0, stage * kXStageBytes);
+    const uint64_t wst = sdesc_at(dw0, stage * (2 * kWStageBytes));
 #pragma unroll
     for (int kk = 0; kk < kBK / 16; ++kk) {
       const uint32_t accum = (kb | kk) != 0;
-      const uint64_t dx = sdesc_k_major(xa + kk * 32, kRowBytes);
+      const uint64_t dx = sdesc_at(xs, kk * 32);
       if (kTokenMajor) {
-        umma_bf16(d, dx, sdesc_k_major(wa + kk * 32, kRowBytes), idesc, accum);
+        umma_bf16(d, dx, sdesc_at(wst, kk * 32), idesc, accum);
       } else {
-        umma_bf16(d, sdesc_k_major(wa + kk * 32, kRowBytes), dx, idesc, accum);
-        umma_bf16(d + 128, sdesc_k_major(wa + kWStageBytes + kk * 32, kRowBytes), dx, idesc,
-                  accum);
+        umma_bf16(d, sdesc_at(wst, kk * 32), dx, idesc, accum);
+        umma_bf16(d + 128, sdesc_at(wst, kWStageBytes + kk * 32), dx, idesc, accum);
       }
     }
     umma_commit(&empty_bar[stage]);
@@ -447,21 +464,20 @@ __device__ __forceinline__ bool single_k_loop(uint32_t d, uint32_t idesc, int nk
 // may hold one), each a 128-row W block (FC1: 64 gate rows, then the 64 up rows of the
 // same channels) and the tile's X rows; one MMA per 16 K, A = the W block, B = X (N = ntok).
 __device__ __forceinline__ bool single_k_loop_narrow(uint32_t d, uint32_t idesc, int nkb,
-                                                     int& stage, uint32_t& phase, uint32_t sx0,
-                                                     uint32_t sw0, uint64_t* full_bar,
+                                                     int& stage, uint32_t& phase, uint64_t dx0,
+                                                     uint64_t dw0, uint64_t* full_bar,
                                                      uint64_t* empty_bar, volatile int* abort) {
   for (int kb = 0; kb < nkb; kb += 2) {
     if (!mbar_wait(&full_bar[stage], phase, abort)) return false;
     tc_fence_after();
-    const uint32_t xa = sx0 + stage * kXStageBytes;
-    const uint32_t wa = sw0 + stage * (2 * kWStageBytes);
+    const uint64_t xs = sdesc_at(dx0, stage * kXStageBytes);
+    const uint64_t wst = sdesc_at(dw0, stage * (2 * kWStageBytes));
     const int nk = nkb - kb < 2 ? 1 : 2;
     for (int b = 0; b < nk; ++b) {
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
-        umma_bf16(d, sdesc_k_major(wa + b * kWStageBytes + kk * 32, kRowBytes),
-                  sdesc_k_major(xa + b * (kXStageBytes / 2) + kk * 32, kRowBytes), idesc,
-                  (kb | b | kk) != 0);
+        umma_bf16(d, sdesc_at(wst, b * kWStageBytes + kk * 32),
+                  sdesc_at(xs, b * (kXStageBytes / 2) + kk * 32), idesc, (kb | b | kk) != 0);
       }
     }
     umma_commit(&empty_bar[stage]);
@@ -782,7 +798,8 @@ __device__ __forceinline__ void single_kernel_body(const SingleMaps& m1, const S
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      const uint32_t sx0 = smem_u32(sX), sw0 = smem_u32(sW);
+      const uint64_t dx0 = sdesc_k_major(smem_u32(sX), kRowBytes);
+      const uint64_t dw0 = sdesc_k_major(smem_u32(sW), kRowBytes);
       for (int it = 0; ok; ++it) {
         const int slot = it & (kSchedDepth - 1);
         if (!mbar_wait(&sched_full[slot], (it / kSchedDepth) & 1, abort)) {
@@ -803,13 +820,13 @@ __device__ __forceinline__ void single_kernel_body(const SingleMaps& m1, const S
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
         const int nkb = t.K / kBK;
         if (kNarrow && t.narrow)
-          ok = single_k_loop_narrow(d, idesc_bf16_f32(128, t.ntok), nkb, stage, phase, sx0, sw0,
+          ok = single_k_loop_narrow(d, idesc_bf16_f32(128, t.ntok), nkb, stage, phase, dx0, dw0,
                                     full_bar, empty_bar, abort);
         else if (t.token_major)
-          ok = single_k_loop<true>(d, idesc_bf16_f32(128, 256), nkb, stage, phase, sx0, sw0,
+          ok = single_k_loop<true>(d, idesc_bf16_f32(128, 256), nkb, stage, phase, dx0, dw0,
                                    full_bar, empty_bar, abort);
         else
-          ok = single_k_loop<false>(d, idesc_bf16_f32(128, t.ntok), nkb, stage, phase, sx0, sw0,
+          ok = single_k_loop<false>(d, idesc_bf16_f32(128, t.ntok), nkb, stage, phase, dx0, dw0,
                                     full_bar, empty_bar, abort);
         if (!ok) {
           flag_timeout(a1.status, abort);
@@ -948,25 +965,33 @@ grouped_gemm_fused_kernel(const __grid_constant__ CUtensorMap f1_x128,
 // per-instruction choice between the two forms cost a quarter of the tensor throughput.
 // Returns false if a stage did not arrive in time.
 template <bool kTokenMajor>
-__device__ __forceinline__ bool pair_k_loop(uint32_t d, uint32_t idesc, int nkb, int& cons,
-                                            uint32_t sx0, uint32_t sw0, uint64_t* full_bar,
-                                            uint64_t* empty_bar, volatile int* abort) {
-  for (int kb = 0; kb < nkb; ++kb) {
-    const int stage = cons % kStages;
-    if (!mbar_wait<true>(&full_bar[stage], (cons / kStages) & 1, abort)) return false;
+__device__ __forceinline__ bool pair_k_loop(uint32_t d, uint32_t idesc, int nkb, int& stage,
+                                            uint32_t& phase, uint64_t dx0, uint64_t dw0,
+                                            uint64_t* full_bar, uint64_t* empty_bar,
+                                            volatile int* abort) {
+  for (int kb = 0; kb < nkb; kb += kPairBlocksPerStage) {
+    if (!mbar_wait<true>(&full_bar[stage], phase, abort)) return false;
     tc_fence_after();
-    const uint32_t xa = sx0 + stage * kXStageBytes;
-    const uint32_t wa = sw0 + stage * kWStageBytes;
+    const int slot0 = stage * kPairBlocksPerStage;
+    const uint64_t xs = sdesc_at(dx0, slot0 * kXStageBytes);
+    const uint64_t wst = sdesc_at(dw0, slot0 * kWStageBytes);
 #pragma unroll
-    for (int kk = 0; kk < kBK / 16; ++kk) {
-      const uint64_t dx = sdesc_k_major(xa + kk * 32, kRowBytes);
-      const uint64_t dw = sdesc_k_major(wa + kk * 32, kRowBytes);
-      if (kTokenMajor) umma_bf16_pair(d, dx, dw, idesc, (kb | kk) != 0);
-      else umma_bf16_pair(d, dw, dx, idesc, (kb | kk) != 0);
+    for (int b = 0; b < kPairBlocksPerStage; ++b) {
+      if (b > 0 && kb + b >= nkb) break;   // an odd block count: the last stage holds one
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        const uint64_t dx = sdesc_at(xs, b * kXStageBytes + kk * 32);
+        const uint64_t dw = sdesc_at(wst, b * kWStageBytes + kk * 32);
+        if (kTokenMajor) umma_bf16_pair(d, dx, dw, idesc, (kb | b | kk) != 0);
+        else umma_bf16_pair(d, dw, dx, idesc, (kb | b | kk) != 0);
+      }
     }
     // The stage is free in both CTAs once these MMAs have read it.
     umma_commit_pair(&empty_bar[stage], kPairMask);
-    ++cons;
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
   }
   return true;
 }
@@ -1008,29 +1033,33 @@ __device__ __forceinline__ bool pair_produce(const Unit& t, const PairMaps& m, c
   const uint32_t tx_bytes = 2u * (xbytes + kWStageBytes);
   const int nkb = t.K / kBK;
   const int claim_kb = nkb > kClaimLead ? nkb - kClaimLead : 0;
-  for (int kb = 0; kb < nkb; ++kb) {
-    if (lead && kb == claim_kb) {
+  for (int kb = 0; kb < nkb; kb += kPairBlocksPerStage) {
+    const int nk = nkb - kb < kPairBlocksPerStage ? nkb - kb : kPairBlocksPerStage;
+    if (lead && claim_kb >= kb && claim_kb < kb + nk) {
       claimed = atomicAdd(sched, 1);
       have_claim = true;
     }
     const int stage = fills % kStages;
     if (!mbar_wait<true>(&empty_bar[stage], ((fills / kStages) & 1) ^ 1u, abort)) return false;
-    if (lead) mbar_arrive_expect_tx(&full_bar[stage], tx_bytes);
-    const int kc = kb * kBK;
+    if (lead) mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>(nk) * tx_bytes);
     const uint32_t fb = lead_full + 8u * stage;
-    uint8_t* xs = sX + stage * kXStageBytes;
-    uint8_t* wsm = sW + stage * kWStageBytes;
-    if (t.token_major) {
-      tma_load_2d_pair(xs, m.x128, fb, kc, xrow);
-      const int wrow = kFc1 ? (lead ? t.n0 : t.N + t.n0) : (t.n0 + 128 * r);
-      tma_load_3d_pair(wsm, mw128, fb, kc, wrow, ecoord);
-    } else {
-      tma_load_2d_pair(xs, m.x64, fb, kc, xrow);
-      if (kFc1) {
-        tma_load_3d_pair(wsm, mw64, fb, kc, t.n0 + 64 * r, ecoord);
-        tma_load_3d_pair(wsm + 64 * kRowBytes, mw64, fb, kc, t.N + t.n0 + 64 * r, ecoord);
+    for (int b = 0; b < nk; ++b) {
+      const int slot = stage * kPairBlocksPerStage + b;
+      const int kc = (kb + b) * kBK;
+      uint8_t* xs = sX + slot * kXStageBytes;
+      uint8_t* wsm = sW + slot * kWStageBytes;
+      if (t.token_major) {
+        tma_load_2d_pair(xs, m.x128, fb, kc, xrow);
+        const int wrow = kFc1 ? (lead ? t.n0 : t.N + t.n0) : (t.n0 + 128 * r);
+        tma_load_3d_pair(wsm, mw128, fb, kc, wrow, ecoord);
       } else {
-        tma_load_3d_pair(wsm, mw128, fb, kc, t.n0 + 128 * r, ecoord);
+        tma_load_2d_pair(xs, m.x64, fb, kc, xrow);
+        if (kFc1) {
+          tma_load_3d_pair(wsm, mw64, fb, kc, t.n0 + 64 * r, ecoord);
+          tma_load_3d_pair(wsm + 64 * kRowBytes, mw64, fb, kc, t.N + t.n0 + 64 * r, ecoord);
+        } else {
+          tma_load_3d_pair(wsm, mw128, fb, kc, t.n0 + 128 * r, ecoord);
+        }
       }
     }
     ++fills;
@@ -1087,9 +1116,9 @@ __device__ __forceinline__ void pair_kernel_body(const PairMaps& m1, const PairM
   // first CTA's shared-memory addresses.
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint8_t* sX = smem;                                   // kStages x up to 128 X rows
-  uint8_t* sW = smem + kStages * kXStageBytes;          // kStages x 128 W rows
-  uint8_t* sOut = sW + kStages * kWStageBytes;          // epilogue staging boxes
+  uint8_t* sX = smem;                                   // kPairSlots x up to 128 X rows
+  uint8_t* sW = smem + kPairSlots * kXStageBytes;       // kPairSlots x 128 W rows
+  uint8_t* sOut = sW + kPairSlots * kWStageBytes;       // epilogue staging boxes
 
   pdl_trigger();
   if (threadIdx.x == 0) {
@@ -1225,11 +1254,13 @@ __device__ __forceinline__ void pair_kernel_body(const PairMaps& m1, const PairM
   } else if (warp == 1) {
     if (lane == 0 && lead) {
       // ------------------------------------------------------------ MMA issuer (first CTA)
-      int cons = 0;
+      int stage = 0;
+      uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      const uint32_t sx0 = smem_u32(sX), sw0 = smem_u32(sW);
+      const uint64_t dx0 = sdesc_k_major(smem_u32(sX), kRowBytes);
+      const uint64_t dw0 = sdesc_k_major(smem_u32(sW), kRowBytes);
       for (int it = 0; ok; ++it) {
         const int slot = it & (kSchedDepth - 1);
         if (!mbar_wait<true>(&sched_full[slot], (it / kSchedDepth) & 1, abort)) {
@@ -1250,10 +1281,10 @@ __device__ __forceinline__ void pair_kernel_body(const PairMaps& m1, const PairM
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kAccCols);
         const int nkb = t.K / kBK;
         ok = t.token_major
-                 ? pair_k_loop<true>(d, idesc_bf16_f32(256, 256), nkb, cons, sx0, sw0, full_bar,
-                                     empty_bar, abort)
-                 : pair_k_loop<false>(d, idesc_bf16_f32(256, t.ntok), nkb, cons, sx0, sw0,
-                                      full_bar, empty_bar, abort);
+                 ? pair_k_loop<true>(d, idesc_bf16_f32(256, 256), nkb, stage, phase, dx0, dw0,
+                                     full_bar, empty_bar, abort)
+                 : pair_k_loop<false>(d, idesc_bf16_f32(256, t.ntok), nkb, stage, phase, dx0,
+                                      dw0, full_bar, empty_bar, abort);
         if (!ok) {
           flag_timeout(a1.status, abort);
           break;
