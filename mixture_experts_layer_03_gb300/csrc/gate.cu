@@ -30,9 +30,14 @@
 namespace moe {
 namespace {
 
-constexpr int kGateBK = 64;                  // K elements per stage
+constexpr int kGateBK = 64;                  // K elements per slot
 constexpr int kGateRowBytes = kGateBK * 2;
-constexpr int kGateMaxStages = 8;
+// The ring holds up to 8 slots of one K block each (an X box and a W box); a pipeline
+// stage is one slot, or two consecutive slots when at least six fit, so that the MMA
+// thread, whose instruction latency (a try_wait, four tiny MMAs and a commit per stage)
+// bounds the K loop, waits and commits once per eight MMAs.
+constexpr int kGateMaxSlots = 8;
+constexpr int kGateMaxStages = kGateMaxSlots;
 constexpr int kGateXBytes = 128 * kGateRowBytes;       // 128 token rows
 constexpr int kGateWMaxBytes = 256 * kGateRowBytes;    // up to 256 gate rows
 constexpr int kGateRingBytes = 4 * (kGateXBytes + kGateWMaxBytes);   // 192 KB of stages
@@ -70,8 +75,9 @@ struct GateArgs {
   int n_col;        // column tiles of 256
   int S;            // CTAs per cluster (K split)
   int box_rows;     // gate rows per tensor-map box (min(256, round_up(E_out, 16)))
-  int stage_bytes;  // X box + W box, rounded up to 1024 (the swizzle atom)
-  int stages;       // ring depth: as many stages as fit in the ring, at most 8
+  int stage_bytes;  // one slot: X box + W box, rounded up to 1024 (the swizzle atom)
+  int per_stage;    // K blocks (slots) per pipeline stage: 1 or 2
+  int stages;       // pipeline stages: as many slots as fit in the ring (at most 8) / per_stage
   uint32_t tmem_cols;
   float* logits;          // [T, E], or NULL (fused routing without the logits written)
   float* shared_logits;   // [T] or NULL
@@ -137,20 +143,28 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
   volatile int* abort = &s_abort;
   pdl_wait();   // x may be the previous kernel's output
 
+  const int G = g.per_stage;
   if (warp == 0 && lane == 0) {
-    // TMA producer over this CTA's K blocks.
+    // TMA producer over this CTA's K blocks, G per stage.
     const uint32_t bytes = static_cast<uint32_t>(kGateXBytes + g.box_rows * kGateRowBytes);
-    int issued = 0;
-    for (int kb = kb0; kb < kb1; ++kb, ++issued) {
-      const int st = issued % g.stages;
-      if (!mbar_wait(&empty_bar[st], ((issued / g.stages) & 1) ^ 1u, abort)) {
+    int issued = 0, st = 0;
+    uint32_t ph = 0;
+    for (int kb = kb0; kb < kb1; kb += G, ++issued) {
+      const int nk = kb1 - kb < G ? kb1 - kb : G;
+      if (!mbar_wait(&empty_bar[st], ph ^ 1u, abort)) {
         *abort = 1;
         break;
       }
-      mbar_arrive_expect_tx(&full_bar[st], bytes);
-      uint8_t* xs = smem + st * g.stage_bytes;
-      tma_load_2d(xs, &map_x, &full_bar[st], kb * kGateBK, row0);
-      tma_load_2d(xs + kGateXBytes, &map_w, &full_bar[st], kb * kGateBK, col0);
+      mbar_arrive_expect_tx(&full_bar[st], static_cast<uint32_t>(nk) * bytes);
+      for (int b = 0; b < nk; ++b) {
+        uint8_t* xs = smem + (st * G + b) * g.stage_bytes;
+        tma_load_2d(xs, &map_x, &full_bar[st], (kb + b) * kGateBK, row0);
+        tma_load_2d(xs + kGateXBytes, &map_w, &full_bar[st], (kb + b) * kGateBK, col0);
+      }
+      if (++st == g.stages) {
+        st = 0;
+        ph ^= 1u;
+      }
     }
     if (*abort) {
       // Let the copies in flight land before shared memory is reused (bounded waits).
@@ -162,20 +176,32 @@ gate_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
   } else if (warp == 1 && lane == 0) {
     // MMA issuer: D[128 tokens, n_mma gate rows] += X . W^T.
     const uint32_t idesc = idesc_bf16_f32(128, n_mma);
-    for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
-      const int st = i % g.stages;
-      if (!mbar_wait(&full_bar[st], (i / g.stages) & 1, abort)) {
+    // Descriptors of slot 0's X and W tiles; a slot's are these plus its offset / 16 (the
+    // start-address field holds shared-address bits 4-17, and the ring lies below 228 KB).
+    const uint64_t dx0 = sdesc_k_major(smem_u32(smem), kGateRowBytes);
+    const uint64_t dw0 = sdesc_k_major(smem_u32(smem) + kGateXBytes, kGateRowBytes);
+    const uint32_t slot_step = static_cast<uint32_t>(g.stage_bytes) >> 4;
+    int st = 0;
+    uint32_t ph = 0;
+    for (int kb = kb0; kb < kb1; kb += G) {
+      const int nk = kb1 - kb < G ? kb1 - kb : G;
+      if (!mbar_wait(&full_bar[st], ph, abort)) {
         *abort = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t xa = smem_u32(smem + st * g.stage_bytes);
-      const uint32_t wa = xa + kGateXBytes;
+      for (int b = 0; b < nk; ++b) {
+        const uint64_t so = static_cast<uint64_t>((st * G + b) * slot_step);
 #pragma unroll
-      for (int kk = 0; kk < kGateBK / 16; ++kk)
-        umma_bf16(tmem, sdesc_k_major(xa + kk * 32, kGateRowBytes),
-                  sdesc_k_major(wa + kk * 32, kGateRowBytes), idesc, (i | kk) != 0);
+        for (int kk = 0; kk < kGateBK / 16; ++kk)
+          umma_bf16(tmem, dx0 + so + 2 * kk, dw0 + so + 2 * kk, idesc,
+                    (kb != kb0 || b != 0 || kk != 0) ? 1u : 0u);
+      }
       umma_commit(&empty_bar[st]);
+      if (++st == g.stages) {
+        st = 0;
+        ph ^= 1u;
+      }
     }
     umma_commit(&acc_bar);   // arrives once every MMA issued above has completed
   }
@@ -306,13 +332,63 @@ cudaError_t gate_smem_optin() {
   return e;
 }
 
+// How many clusters of S CTAs of one instantiation can be resident at once, once per device
+// and S (0 if the query fails: then no limit is applied).
+template <int EPL, int kRoute>
+int gate_max_clusters(int S) {
+  static std::atomic<int> known[64][4];   // value + 1; 0 = not yet queried
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int si = S <= 1 ? 0 : S == 2 ? 1 : S == 4 ? 2 : 3;
+  const bool cache = dev >= 0 && dev < 64;
+  if (cache) {
+    const int v = known[dev][si].load(std::memory_order_acquire);
+    if (v) return v - 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(S));
+  cfg.blockDim = dim3(gate_threads(kRoute));
+  cfg.dynamicSmemBytes = kGateSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gate_kernel<EPL, kRoute>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  if (cache) known[dev][si].store(n + 1, std::memory_order_release);
+  return n;
+}
+
 template <int EPL, int kRoute>
 cudaError_t launch_gate_t(const cudaLaunchConfig_t& cfg0, const CUtensorMap& mx,
-                          const CUtensorMap& mw, const GateArgs& g) {
+                          const CUtensorMap& mw, const GateArgs& g0) {
   const cudaError_t e = gate_smem_optin<EPL, kRoute>();
   if (e != cudaSuccess) return e;
+  // All clusters resident at once: clusters that do not fit wait for a second wave (16
+  // clusters of 8 CTAs started up to 9 us apart). Halve the K split until they fit.
+  GateArgs g = g0;
+  const int clusters = static_cast<int>(cfg0.gridDim.x) / g.S;
+  while (g.S > 1) {
+    const int fit = gate_max_clusters<EPL, kRoute>(g.S);
+    if (fit == 0 || clusters <= fit) break;
+    g.S >>= 1;
+  }
   cudaLaunchConfig_t cfg = cfg0;
   cfg.blockDim = dim3(gate_threads(kRoute));
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * g.S));
+  cudaLaunchAttribute attr[2];
+  for (unsigned i = 0; i < cfg0.numAttrs && i < 2; ++i) {
+    attr[i] = cfg0.attrs[i];
+    if (attr[i].id == cudaLaunchAttributeClusterDimension)
+      attr[i].val.clusterDim.x = static_cast<unsigned>(g.S);
+  }
+  cfg.attrs = attr;
   return cudaLaunchKernelEx(&cfg, gate_kernel<EPL, kRoute>, mx, mw, g);
 }
 
@@ -347,8 +423,10 @@ moe_status launch_gate(const void* x, const void* wg, int64_t T, int H, int E, i
   const int e16 = (g.E_out + 15) & ~15;
   g.box_rows = e16 < 256 ? e16 : 256;
   g.stage_bytes = (kGateXBytes + g.box_rows * kGateRowBytes + 1023) & ~1023;
-  g.stages = kGateRingBytes / g.stage_bytes;
-  if (g.stages > kGateMaxStages) g.stages = kGateMaxStages;
+  int slots = kGateRingBytes / g.stage_bytes;
+  if (slots > kGateMaxSlots) slots = kGateMaxSlots;
+  g.per_stage = slots >= 6 ? 2 : 1;
+  g.stages = slots / g.per_stage;
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(g.box_rows)) cols <<= 1;
   g.tmem_cols = cols;
