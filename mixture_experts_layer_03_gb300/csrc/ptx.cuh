@@ -285,15 +285,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// As umma_commit, arriving on the barrier at the same offset in every CTA in `mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
 // ---- CTA-pair (cta_group::2) forms: one MMA spans the two CTAs of a cluster pair.
 // A (M = 256) takes rows 0-127 from the first CTA's shared memory and 128-255 from the
 // second's, at the same offsets; B (N) takes columns [0, N/2) from the first CTA and
