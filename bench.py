@@ -15,6 +15,7 @@ collective) and the job value is the tokens of all ranks over the slowest rank's
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -80,35 +81,55 @@ def load_peaks():
 # --------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+    """nvidia-smi samples every 20 ms, each with its timestamp; `summary` keeps those taken
+    inside the window marked by `mark_start` / `mark_end` (the timed region), and falls
+    back to every sample when none falls inside."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.t0 = self.t1 = None
         self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
         time.sleep(0.3)
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(2 * self.INTERVAL_MS / 1000)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+
+    @staticmethod
+    def _stamp(text: str):
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
 
     def summary(self):
         self.out.flush()
@@ -121,25 +142,35 @@ class ClockSampler:
                 os.unlink(self.out.name)
             except OSError:
                 pass
-        sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
+                sm, smax = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+            try:
+                watts = float(parts[4])
+            except ValueError:
+                watts = None
+            why = {n for n, v in zip(names, parts[6:10]) if v.lower() == "active"}
+            rows.append((self._stamp(parts[0]), sm, smax, watts, why))
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [r for r in rows if r[0] is not None and self.t0 is not None and self.t1 is not None
+                  and self.t0 <= r[0] <= self.t1]
+        use = inside or rows
+        power = [r[3] for r in use if r[3] is not None]
+        out = {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": use[-1][2],
+               "reasons": sorted(set().union(*(r[4] for r in use))), "samples": len(use),
+               "window": "timed region" if inside else "whole sampling run (no sample fell inside the timed region)",
+               "interval_ms": self.INTERVAL_MS}
+        if power:
+            out["power_w"] = round(statistics.median(power), 1)
+        return out
 
 
 # --------------------------------------------------------------------------- CPU oracle
@@ -364,6 +395,7 @@ def measure(name: str, args, rank: int, world: int, dev, headline: bool) -> dict
           for _ in range(args.steps)]
     with ClockSampler(dev.index) as clk:
         barrier()
+        clk.mark_start()
         torch.cuda._sleep(20_000_000)
         for i in range(args.steps):
             flush(i)
@@ -371,6 +403,7 @@ def measure(name: str, args, rank: int, world: int, dev, headline: bool) -> dict
             graph.replay()
             ev[i][1].record(stream)
         barrier()
+        clk.mark_end()
     clocks = clk.summary()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = reduce_max(sum(step_ms), world, dev)
