@@ -382,6 +382,9 @@ GATE_TOL = 1e-4   # fp32 accumulation of H bf16 products, relative to max|logit|
     (4096, 4096, 8, 0, RENORMALIZE_NAIVE),    # mixtral_prefill's gate
     (100, 512, 2, 1, RENORMALIZE_NAIVE),      # 3 gate rows (padded to 4), FSE row last
     (77, 256, 15, 1, RENORMALIZE_NAIVE),      # 16 rows, one 16-row MMA tile
+    (100, 448, 8, 0, RENORMALIZE_NAIVE),      # 7 K blocks over 2 CTAs: a stage holding one
+    (2048, 5120, 16, 1, LLAMA4),              # llama4_scout's gate: 16 clusters of 8 do not
+                                              # all fit, the K split drops to 4
 ])
 def test_gate_parity_and_routing_on_its_logits(moe, T, H, E, ns, method):
     g = torch.Generator().manual_seed(T + E)
@@ -425,6 +428,8 @@ GATE_ROUTE_CASES = [
     (300, 128, 16, 0, RENORMALIZE_NAIVE, 4, {}, True),         # integer logits: ties
     (300, 128, 16, 0, DEEPSEEKV3, 4, dict(n_group=4, topk_group=2), True),
     (300, 128, 32, 0, GROUPED_TOPK, 4, dict(n_group=8, topk_group=2), True),
+    (2048, 5120, 16, 1, LLAMA4, 1, {}, False),                 # llama4_scout's gate (K split 4)
+    (100, 448, 8, 0, RENORMALIZE_NAIVE, 2, {}, False),         # a stage holding one K block
 ]
 
 
