@@ -272,6 +272,8 @@ SMALL_CASES = [
     (1100, 256, 256, 4, 1, 0, "one_expert"),   # CTA pairs: 4 units + 76 rows (weight-major)
     (1200, 384, 320, 4, 1, 0, "one_expert"),   # CTA pairs: 4 units + 176 rows (masked pair)
     (1034, 256, 192, 4, 1, 0, "one_expert"),   # CTA pairs: 4 units + 10 rows (64-row X box, 8 used)
+    (1100, 192, 192, 4, 1, 0, "one_expert"),   # CTA pairs, 3 K blocks in FC1 and FC2: a stage
+                                               # holding one block at the end of every unit
     (150, 256, 192, 4, 1, 0, "one_expert"),    # single-SM: 1 full tile + 22 rows (16-row X boxes)
     (180, 256, 192, 4, 1, 0, "one_expert"),    # single-SM: 1 full tile + 52 rows (64-row X box)
     (2200, 256, 192, 4, 2, 256, "route"),      # CTA pairs for routed and shared groups
