@@ -276,6 +276,8 @@ SMALL_CASES = [
                                                # holding one block at the end of every unit
     (150, 256, 192, 4, 1, 0, "one_expert"),    # single-SM: 1 full tile + 22 rows (16-row X boxes)
     (180, 256, 192, 4, 1, 0, "one_expert"),    # single-SM: 1 full tile + 52 rows (64-row X box)
+    (300, 128, 64, 2, 1, 0, "one_expert"),     # single-SM: 2 full tiles + 44 rows; FC1's one
+                                               # channel tile half past I = 64
     (2200, 256, 192, 4, 2, 256, "route"),      # CTA pairs for routed and shared groups
     # CTA-pair weight-major leftover units of 1, 16, 32, 33 and 128 rows beside full units
     (640, 512, 320, 2, 2, 0, "one_expert"),    # 2 full units + 128 rows, ragged FC1 tile
