@@ -35,7 +35,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from workloads import WORKLOADS, Workload, make_inputs, flops, min_bytes  # noqa: E402
+from workloads import WORKLOADS, Workload, make_inputs, flops, min_bytes, pipeline_bytes  # noqa: E402
 
 METRIC = "MoE layer tokens/sec at 1 GB300 and % of roofline (HBM or bf16 TC)"
 UNIT = "tokens/s"
@@ -602,6 +602,11 @@ def measure(name: str, args, rank: int, world: int, dev, headline: bool) -> dict
              "achieved_gbs": round(by / (ms_per_step * 1e-3) / 1e9, 1),
              "peaks": f"{peak_src}: hbm_gbs {peaks['hbm_gbs']}, bf16_tflops (burst) "
                       f"{peaks['bf16_tflops']}"}
+    # Diagnostic: the bytes the permuted pipeline moves (x_perm, h and out_perm round trips
+    # on top of `bytes`) and their time at the measured copy bandwidth.
+    pb = pipeline_bytes(w, n_active)
+    layer["pipeline_bytes"] = pb
+    layer["pipeline_t_hbm_ms"] = round(pb / (peaks["hbm_gbs"] * 1e9) * 1e3, 4)
 
     if not headline:
         return {"ms_per_step": round(ms_per_step, 4), "tokens_per_s": round(value, 1),

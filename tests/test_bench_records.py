@@ -1,5 +1,5 @@
-"""The bench's clock record: nvidia-smi samples parsed, and only those inside the timed
-region kept (host logic, no GPU)."""
+"""Host logic of the bench's records (no GPU): the clock record keeps only the nvidia-smi
+samples taken inside the timed region; the roofline byte counts equal their closed forms."""
 import datetime
 import os
 import sys
@@ -49,3 +49,21 @@ def test_falls_back_to_every_sample_when_none_is_inside():
 def test_no_samples_gives_an_empty_record():
     out = _sampler(["garbage\n", "1, 2\n"], 0.0, 1.0).summary()
     assert out == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_roofline_byte_counts_match_their_closed_forms():
+    """The layer roofline's algorithmic bytes and the pipeline-bytes diagnostic, written
+    out for mixtral_prefill (8 active experts) and dsv3_layer (shared expert)."""
+    from workloads import WORKLOADS, min_bytes, pipeline_bytes
+    w = WORKLOADS["mixtral_prefill"]
+    T, H, I, E, k = 4096, 4096, 14336, 8, 2
+    alg = 8 * 3 * H * I * 2 + 2 * T * H * 2 + T * E * 4 + T * k * 8
+    assert min_bytes(w, 8) == alg
+    P = T * k
+    assert pipeline_bytes(w, 8) == alg + 5 * P * H * 2 + 2 * P * I * 2
+    w = WORKLOADS["dsv3_layer"]
+    T, H, I, E, k, Is = 512, 7168, 2048, 256, 8, 2048
+    alg = 256 * 3 * H * I * 2 + 3 * H * Is * 2 + 2 * T * H * 2 + T * E * 4 + T * k * 8
+    assert min_bytes(w, 256) == alg
+    P = T * k
+    assert pipeline_bytes(w, 256) == alg + 5 * (P + T) * H * 2 + 2 * (P * I + T * Is) * 2

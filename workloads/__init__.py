@@ -160,6 +160,17 @@ def min_bytes(w: Workload, n_active: int) -> float:
             + 2 * w.T * w.H * wb + w.T * w.E * 4 + w.T * w.k * 8)
 
 
+def pipeline_bytes(w: Workload, n_active: int) -> float:
+    """What the permuted pipeline moves beyond `min_bytes`: x rows read and written into
+    x_perm and read back by FC1, h written by FC1 and read by FC2, out_perm written by FC2
+    and read by finalize, for the P routed rows (and the T shared-expert rows). A
+    diagnostic beside the roofline, which counts `min_bytes` only."""
+    wb = 2
+    rows_r, rows_s = w.P, (w.T if w.shared_I else 0)
+    return (min_bytes(w, n_active) + 5 * (rows_r + rows_s) * w.H * wb
+            + 2 * (rows_r * w.I + rows_s * w.shared_I) * wb)
+
+
 __all__ = ["Workload", "WORKLOADS", "ORDER", "make_inputs", "small_case", "zipf_logit_bias",
-           "flops", "min_bytes", "DEFAULT", "RENORMALIZE", "DEEPSEEKV3", "LLAMA4",
+           "flops", "min_bytes", "pipeline_bytes", "DEFAULT", "RENORMALIZE", "DEEPSEEKV3", "LLAMA4",
            "RENORMALIZE_NAIVE", "MINIMAX2", "SIGMOID_RENORM", "GROUPED_TOPK"]
