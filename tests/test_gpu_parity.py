@@ -298,7 +298,30 @@ SMALL_CASES = [
 ]
 
 
-@pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: "T{}H{}I{}E{}k{}s{}-{}".format(*c))
+def _random_cases(n, seed):
+    """Seeded random shapes inside the envelope: H and I multiples of 64 up to 512, up to
+    64 experts, k up to 8, up to 1200 tokens, with and without a shared expert, each with
+    routed, duplicated-random or single-expert ids. Together they land on every GEMM form
+    (CTA pairs, single-SM tiles, narrow tiles) with ragged group sizes."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        H = 64 * int(rng.integers(1, 9))
+        I = 64 * int(rng.integers(1, 9))
+        E = int(rng.choice([1, 2, 3, 5, 8, 16, 33, 64]))
+        mode = str(rng.choice(["route", "route", "random_dup", "one_expert"]))
+        k = int(rng.integers(1, (min(8, E) if mode != "random_dup" else 8) + 1))
+        T = int(rng.integers(1, 1201))
+        sI = int(rng.choice([0, 0, 64, 192]))
+        cases.append((T, H, I, E, k, sI, mode))
+    return cases
+
+
+RANDOM_CASES = _random_cases(20, 2026)
+
+
+@pytest.mark.parametrize("case", SMALL_CASES + RANDOM_CASES,
+                         ids=lambda c: "T{}H{}I{}E{}k{}s{}-{}".format(*c))
 def test_forward_steps_parity(moe, case):
     T, H, I, E, k, sI, mode = case
     c = _random_case(T, H, I, E, k, sI, seed=T + H, ids_mode=mode)
