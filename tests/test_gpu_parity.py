@@ -84,7 +84,47 @@ ROUTE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("case", ROUTE_CASES, ids=lambda c: f"T{c[0]}E{c[1]}k{c[2]}m{c[3]}")
+def _random_route_cases(n, seed):
+    """Seeded random routing problems inside the envelope, every method, with random valid
+    group parameters for the grouped ones; half of them draw integer logits (exact ties in
+    logits, keys and group scores)."""
+    rng = np.random.default_rng(seed)
+    methods = [DEFAULT, RENORMALIZE, DEEPSEEKV3, LLAMA4, RENORMALIZE_NAIVE, MINIMAX2,
+               SIGMOID_RENORM, GROUPED_TOPK]
+    cases = []
+    for i in range(n):
+        method = methods[i % len(methods)]
+        T = int(rng.integers(1, 600))
+        ng, tg, rsf = 1, 1, 1.0
+        if method == DEEPSEEKV3:
+            ng = int(rng.choice([1, 2, 4, 8, 16]))
+            epg = int(rng.integers(2, min(32, 256 // ng) + 1))
+            E = ng * epg
+            tg = int(rng.integers(1, ng + 1))
+            while epg * tg > 256:
+                tg -= 1
+            k = int(rng.integers(1, min(8, epg * tg) + 1))
+            rsf = float(rng.choice([1.0, 2.5]))
+        elif method == GROUPED_TOPK:
+            ng = int(rng.choice([1, 2, 4, 8, 16, 32]))
+            epg = int(rng.integers(1, max(1, 256 // ng) + 1))
+            E = ng * epg
+            tg = int(rng.integers(1, min(ng, 8) + 1))
+            per = int(rng.integers(1, min(epg, 8 // tg) + 1))
+            k = per * tg
+            rsf = float(rng.choice([1.0, 2.5]))
+        else:
+            E = int(rng.integers(1, 257))
+            k = int(rng.integers(1, min(8, E) + 1))
+        cases.append((T, E, k, method, ng, tg, rsf, 1.0, bool(i % 2)))
+    return cases
+
+
+RANDOM_ROUTE_CASES = _random_route_cases(40, 77)
+
+
+@pytest.mark.parametrize("case", ROUTE_CASES + RANDOM_ROUTE_CASES,
+                         ids=lambda c: f"T{c[0]}E{c[1]}k{c[2]}m{c[3]}g{c[4]}-{c[5]}{'-int' if c[8] else ''}")
 def test_route_parity(moe, case):
     T, E, k, method, ng, tg, rsf, scale, int_logits = case
     g = torch.Generator().manual_seed(11)
