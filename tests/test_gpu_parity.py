@@ -533,6 +533,48 @@ def test_gate_route_fused(moe, case):
     np.testing.assert_allclose(sc.cpu().numpy(), sc_ref, rtol=1e-6, atol=0)
 
 
+def _random_gate_cases(n, seed):
+    """Seeded random gate problems: T up to 2500, H up to 3072, the routing problems of
+    _random_route_cases, with or without the shared expert's gate row."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for (_, E, k, method, ng, tg, rsf, _, _) in _random_route_cases(n, seed + 1):
+        T = int(rng.integers(1, 2501))
+        H = 64 * int(rng.integers(1, 49))
+        ns = int(rng.integers(0, 2))
+        kw = {} if method not in (DEEPSEEKV3, GROUPED_TOPK) else dict(
+            n_group=ng, topk_group=tg, routed_scaling_factor=rsf)
+        cases.append((T, H, E, ns, method, k, kw))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_gate_cases(16, 303),
+                         ids=lambda c: "T{}H{}E{}s{}m{}k{}".format(*c[:6]))
+def test_gate_random_shapes(moe, case):
+    """Random gate shapes (K split, cluster size, stage grouping and column tiles vary with
+    them): the logits against the oracle's gate, the fused routing against the route
+    kernel on those logits bit for bit, and ids bit-exact against the oracle."""
+    T, H, E, ns, method, k, kw = case
+    g = torch.Generator().manual_seed(T * 7 + H + E)
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    wg = (torch.randn(E + ns, H, generator=g) * H ** -0.5).to(torch.bfloat16)
+    bias = (torch.randn(E, generator=g) * 0.1).cuda() if method in (DEEPSEEKV3, MINIMAX2) else None
+    lg, sg = moe.moe_gate(x.cuda(), wg.cuda(), E)
+    ids, sc, _, _ = moe.moe_gate_route(x.cuda(), wg.cuda(), method, k, E, bias=bias, **kw)
+    torch.cuda.synchronize()
+    ref_r, ref_s = oracle.gate(_np64(x), _np64(wg), E)
+    _check_close(lg.cpu().double().numpy(), ref_r, GATE_TOL, "routed logits")
+    if ns:
+        _check_close(sg.cpu().double().numpy(), ref_s, GATE_TOL, "shared gate logits")
+    ids_r, sc_r = moe.moe_route(lg, method, k, bias=bias, **kw)
+    assert torch.equal(ids, ids_r)
+    assert torch.equal(sc.view(torch.int32), sc_r.view(torch.int32))
+    ids_ref, sc_ref = oracle.route(lg.cpu().numpy(), method, k,
+                                   bias=None if bias is None else bias.cpu().numpy(), **kw)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(sc.cpu().numpy(), sc_ref, rtol=1e-6, atol=0)
+
+
 def test_forward_with_the_fused_shared_gate(moe):
     T, H, I, E, k, sI = 300, 256, 192, 8, 2, 128
     c = _random_case(T, H, I, E, k, sI, seed=5)
